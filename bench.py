@@ -1,0 +1,382 @@
+"""Benchmark of the MoE decode hot path on the Kimi-K2-shaped layer.
+
+Workload: one MoE decode step = route 1 token over 384 experts (top-8, fp32
+logits), rotate its bf16 [1, 7168] input, gate||up gather-qmv over the 8
+routed ternary experts (group 16, 20 trits per word), SwiGLU + rotation of the
+2048-wide intermediate, down multi-gather-qmv, router-weighted combine.  The
+metric is packed-weight bytes read per second by the step (codes + fp16 scales
+of the 8 routed experts, 114,720,768 B per step).
+
+Timing: inputs resident in HBM; each timed step is one CUDA-graph replay of the
+whole step between two CUDA events, with a 256 MiB L2 flush before every step
+(outside the events) and a 5.5 GB expert bank, so every step reads its experts
+from HBM.  ``e2e`` repeats the step through the Python API with the step's
+inputs copied from pinned host memory and its output copied back.
+
+Also measured: the gate||up gather-qmv launch alone (roofline of the dominant
+kernel), and the fp64 oracle on a bounded sample on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+E, TOPK, HIDDEN, INTER, GROUP = 384, 8, 7168, 2048, 16
+SEED = 3
+
+
+def packed_bytes_per_expert():
+    """Algorithmic bytes of one expert: unpadded code words + fp16 scales, gate||up and down."""
+    gu_words = -(-HIDDEN // 20)  # 359
+    dn_words = -(-INTER // 20)   # 103
+    gu = 2 * INTER * (gu_words * 4 + (HIDDEN // GROUP) * 2)
+    dn = HIDDEN * (dn_words * 4 + (INTER // GROUP) * 2)
+    return gu, dn
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- oracle on the host
+
+def oracle_sample(seconds: float, rows_per_expert: int = 48):
+    """Time the fp64 oracle's decode-matvec on sampled rows of routed experts.
+
+    Returns (bytes processed, seconds, description).  Runs single-threaded
+    numpy; the packed words are drawn like the device timing bank."""
+    import numpy as np
+
+    from oracle import tq_oracle as o
+    from rotated_codebook_quantized_gb300 import workloads as wl
+
+    c3, _ = o.lloyd_max_gaussian(3)
+    g = wl.rng(SEED, 77)
+    _, x = wl.activations(SEED, 1, HIDDEN)
+    signs = o.rotation_signs(wl.sign_seed(SEED, 0), HIDDEN)
+    xr = o.rotate(x, signs, o.rotation_block(HIDDEN))[0]
+    h = g.normal(size=INTER)
+    gu_row = (-(-HIDDEN // 20)) * 4 + (HIDDEN // GROUP) * 2
+    dn_row = (-(-INTER // 20)) * 4 + (INTER // GROUP) * 2
+    done_bytes, t0, steps = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < seconds or steps == 0:
+        logits = wl.router_logits(SEED, 1, E) + steps
+        ids, probs = o.route(logits, TOPK)
+        for e in ids[0]:
+            wgu = g.integers(0, 3 ** 20, size=(rows_per_expert, -(-HIDDEN // 20)), dtype=np.int64).astype(np.uint32)
+            sgu = np.exp(g.normal(-3.5, 0.5, size=(rows_per_expert, HIDDEN // GROUP))).astype(np.float16)
+            wdn = g.integers(0, 3 ** 20, size=(rows_per_expert, -(-INTER // 20)), dtype=np.int64).astype(np.uint32)
+            sdn = np.exp(g.normal(-3.5, 0.5, size=(rows_per_expert, INTER // GROUP))).astype(np.float16)
+            o.qmv(o.dequantize(o.unpack(wgu, 3, HIDDEN), sgu, c3, GROUP), xr[None])
+            o.qmv(o.dequantize(o.unpack(wdn, 3, INTER), sdn, c3, GROUP), h[None])
+            done_bytes += rows_per_expert * (gu_row + dn_row)
+        steps += 1
+    dt = time.perf_counter() - t0
+    desc = (f"fp64 oracle decode-matvec (unpack, dequantize, matvec) of {rows_per_expert} gate||up rows and "
+            f"{rows_per_expert} down rows of each of the 8 routed experts, {steps} routed steps, single thread")
+    return done_bytes, dt, desc
+
+
+def cpu_baseline_subprocess(seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(seconds)],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "oracle sample failed"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": d["desc"]}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- device bank
+
+def make_bank(torch, tq, dev):
+    """Timing bank of 384 ternary experts with random valid words and fp16 scales (device-generated)."""
+    cb = tq.Codebook(3, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + SEED)
+    gu_stride = tq.row_stride_words(3, HIDDEN)  # 360
+    dn_stride = tq.row_stride_words(3, INTER)   # 104
+    gu_codes = torch.empty((E, 2 * INTER, gu_stride), dtype=torch.int32, device=dev)
+    dn_codes = torch.empty((E, HIDDEN, dn_stride), dtype=torch.int32, device=dev)
+    gu_sc = torch.empty((E, 2 * INTER, HIDDEN // GROUP), dtype=torch.float16, device=dev)
+    dn_sc = torch.empty((E, HIDDEN, INTER // GROUP), dtype=torch.float16, device=dev)
+    for e in range(E):
+        for codes, K in ((gu_codes[e], HIDDEN), (dn_codes[e], INTER)):
+            nw = -(-K // 20)
+            w = torch.randint(0, 3 ** 20, codes[:, :nw].shape, generator=gen, device=dev, dtype=torch.int64)
+            used = K - (nw - 1) * 20
+            w[:, -1] %= 3 ** used
+            codes[:, :nw] = (w - (w >= 2 ** 31).long() * 2 ** 32).to(torch.int32)
+            codes[:, nw:] = 0
+        for sc in (gu_sc[e], dn_sc[e]):
+            sc.copy_(torch.exp(torch.randn(sc.shape, generator=gen, device=dev) * 0.5 - 3.5))
+    qgu = tq.QWeight(gu_codes, gu_sc.view(torch.int16), E, 2 * INTER, HIDDEN, GROUP, cb, row_stride=gu_stride)
+    qdn = tq.QWeight(dn_codes, dn_sc.view(torch.int16), E, HIDDEN, INTER, GROUP, cb, row_stride=dn_stride)
+    return qgu, qdn
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--_oracle-sample", dest="oracle_sample", type=float, default=None)
+    args = ap.parse_args()
+
+    if args.oracle_sample is not None:
+        b, s, desc = oracle_sample(args.oracle_sample)
+        print(json.dumps({"bytes": b, "seconds": s, "desc": desc}))
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    gu_b, dn_b = packed_bytes_per_expert()
+    step_bytes = TOPK * (gu_b + dn_b)
+    config = {"workload": "MoE decode layer, Kimi-K2-shaped: 384 experts, top-8, hidden 7168, expert intermediate "
+                          "2048, ternary group 16 (gate||up gather_qmv + SwiGLU/rotate + down multi_gather_qmv)",
+              "experts": E, "top_k": TOPK, "hidden": HIDDEN, "intermediate": INTER, "group": GROUP,
+              "tokens_per_step": 1, "bytes_per_step": step_bytes,
+              "cache": "L2 flushed (256 MiB write) before every timed step; 5.5 GB expert bank, fresh routing per step"}
+    metric = "MoE gather_qmv decode packed-weight GB/s"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per = []
+        total_b = total_s = 0.0
+        for i in range(args.warmup + args.steps):
+            b, s, desc = oracle_sample(0.0, rows_per_expert=16)
+            if i >= args.warmup:
+                total_b += b
+                total_s += s
+        value = total_b / total_s / 1e9
+        print(json.dumps({"impl": "reference", "metric": metric, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    cpu = cpu_baseline_subprocess(args.cpu_seconds) if rank == 0 else None
+
+    import torch
+
+    import rotated_codebook_quantized_gb300 as tq
+    from rotated_codebook_quantized_gb300 import workloads as wl
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tq.load()
+    peaks = measured_peaks()
+
+    qgu, qdn = make_bank(torch, tq, dev)
+    rotH = tq.Rotation(HIDDEN, 1024, seed=wl.sign_seed(SEED, 0), device=dev)
+    rotI = tq.Rotation(INTER, 2048, seed=wl.sign_seed(SEED, 1), device=dev)
+    nsteps = args.warmup + args.steps
+    logits_all = torch.from_numpy(wl.router_logits(SEED + 17 * rank, nsteps, E)).to(dev)
+    x_all = torch.from_numpy(wl.activations(SEED + 17 * rank, nsteps, HIDDEN)[0].view("int16")).to(dev).view(
+        torch.bfloat16)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    logits_buf = torch.empty((1, E), dtype=torch.float32, device=dev)
+    x_buf = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK)
+        xr = tq.rotate(x_buf, rotH)
+        gu = tq.gather_qmv(qgu, xr, ids)
+        hr = tq.swiglu_rotate(gu, INTER, rotI)
+        yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
+        return tq.moe_combine(yd, probs, TOPK)
+
+    launches_per_step = 8  # route: top-k, scan, compact; rotate; gather; swiglu+rotate; multi-gather; combine
+
+    # warm up eagerly (first calls set kernel attributes), then capture the step
+    logits_buf.copy_(logits_all[0:1])
+    x_buf.copy_(x_all[0:1])
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            out_static = step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(nsteps):
+            flush.fill_(i & 0xFF)
+            logits_buf.copy_(logits_all[i:i + 1])
+            x_buf.copy_(x_all[i:i + 1])
+            ev[i][0].record()
+            g.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier()
+    times = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
+    t_ms = sum(times)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    value = world * args.steps * step_bytes / (t_ms * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    # dominant kernel alone: gate||up gather_qmv, one launch per replay, L2 flushed between
+    ids_fixed = torch.tensor([[3, 77, 120, 191, 250, 301, 333, 383]], dtype=torch.int32, device=dev)
+    xr_fixed = tq.rotate(x_all[0:1], rotH)
+    gs = torch.cuda.Stream(device=dev)
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg, stream=gs):
+            tq.gather_qmv(qgu, xr_fixed, ids_fixed)
+    torch.cuda.current_stream().wait_stream(gs)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
+    for i in range(40):
+        flush.fill_(i & 0xFF)
+        kev[i][0].record()
+        kg.replay()
+        kev[i][1].record()
+    torch.cuda.synchronize()
+    kt = sorted(kev[i][0].elapsed_time(kev[i][1]) for i in range(5, 40))
+    k_ms = sum(kt) / len(kt)
+    k_bytes = TOPK * gu_b
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    roofline = {"kernel": "qmv_kernel<3,16,1> (gate||up gather_qmv, 8 experts)", "bound": "hbm",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
+                "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_ms * 1e3}
+    tr = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr):
+        d = json.load(open(tr)).get("gather_qmv_gate_up")
+        if d:
+            roofline["traffic"] = d
+
+    # end to end through the Python API: pinned host inputs in, result out, every step
+    h_logits = torch.from_numpy(wl.router_logits(SEED + 17 * rank + 5, nsteps, E)).pin_memory()
+    h_x = torch.from_numpy(wl.activations(SEED + 17 * rank + 5, nsteps, HIDDEN)[0].view("int16")).pin_memory()
+    h_out = torch.empty((nsteps, HIDDEN), dtype=torch.float32).pin_memory()
+    d_x = torch.empty((1, HIDDEN), dtype=torch.int16, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(nsteps):
+        if i == args.warmup:
+            barrier()
+            e0.record()
+        logits_buf.copy_(h_logits[i:i + 1], non_blocking=True)
+        d_x.copy_(h_x[i:i + 1], non_blocking=True)
+        x_buf.copy_(d_x.view(torch.bfloat16))
+        out = step()
+        h_out[i:i + 1].copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": E * 4 + HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
+           "ms_per_step": e2e_ms / args.steps}
+
+    if rank == 0:
+        line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+                "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+                "wall_s_timed_loop": wall}
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,294 @@
+/*
+ * tq.h -- C ABI of the rotated-codebook quantization library (libtq.so).
+ *
+ * The method (TurboQuant-style weight and KV-cache quantization) as stated on
+ * the page "How it works" (turboquant-mlx), sections
+ *   "Quantizing a weight, with no data"   rotate, group + RMS scale, snap, pack
+ *   "The ternary tier (1.58 bits)"        {-c, 0, +c}, 20 trits per 32-bit word
+ *   "Running a quantized layer"           rotate the input, decode codes inline;
+ *                                         the MoE kernel split by shape of work
+ *   "The KV cache"                        same rotation + codebook, 8-bit K / 3-bit V
+ *   "Configuration that converter and loader share"
+ *                                         codebook size marks bit vs trit packing
+ * and on the page "Running a 1T-Parameter Model on a Laptop" (the MoE router,
+ * create_hadamard_matrix, the TurboQuant KV cache update_and_fetch).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument documented as "device" is a CUDA device pointer
+ *    owned by the caller; the library allocates no memory and keeps no state.
+ *    "host" pointers are ordinary CPU memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *    work is enqueued asynchronously on it; the call returns once enqueued.
+ *  - Return value: TQ_OK, or an error found on the host before any launch
+ *    (TQ_ERR_INVALID: bad argument; TQ_ERR_UNSUPPORTED: valid but not built)
+ *    or a launch error (TQ_ERR_CUDA).  Nothing is launched when a host check
+ *    fails.
+ *  - Errors a kernel detects (an expert id out of range, a bounded wait that
+ *    ran out, a codebook of the wrong shape) are OR-ed as TQ_DEVERR_* bits into
+ *    the optional device word `err` (NULL: not reported).  The offending rows
+ *    are written as zeros; no kernel traps.
+ *  - Codes: a codebook of 3 entries means trit-packed (20 base-3 digits per
+ *    uint32, digit j has weight 3^j); 2^b entries (b = 1,2,3,4,8) means
+ *    bit-packed, 32/b codes per word (10 for b = 3, top two bits zero), code j
+ *    of a word at bits [b*j, b*j+b).  Each row starts a fresh word; unused
+ *    slots and padding words are zero.  Digit/code value i stands for the
+ *    i-th centroid in ascending order.
+ *  - Scales: IEEE fp16 bit patterns, one per group of `group` consecutive
+ *    codes of a row, row-major [rows, cols/group].
+ *  - Rotation: R = blockdiag(H_b, ..., H_b) . diag(signs) / sqrt(b), H_b the
+ *    Sylvester Hadamard matrix of order b (a power of two dividing dim).
+ *    Weights are stored rotated along the input dim (W_rot = W R^T), so
+ *    W x = W_rot (R x).
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tq_status {
+    TQ_OK = 0,
+    TQ_ERR_INVALID = 1,      /* argument rejected on the host */
+    TQ_ERR_UNSUPPORTED = 2,  /* valid combination that this build does not cover */
+    TQ_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    TQ_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (from tq_check_error) */
+    TQ_ERR_DEVICE = 5        /* a kernel reported a bad input (from tq_check_error) */
+} tq_status;
+
+/* Bits of the device error word. */
+#define TQ_DEVERR_BAD_ID 1u      /* an expert id outside [0, experts) */
+#define TQ_DEVERR_TIMEOUT 2u     /* a bounded spin-wait gave up */
+#define TQ_DEVERR_BAD_BOOK 4u    /* a ternary codebook that is not {c0, c0+d, c0+2d} */
+
+typedef enum tq_dtype { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+/* A codebook in device memory.  levels: 3, or 2^b with b in {1,2,3,4,8}.
+ * centroids: device float[levels], ascending.  thresholds: device
+ * float[levels-1], ascending; thresholds[i] separates centroids i and i+1
+ * (the midpoints for a Lloyd-Max book). */
+typedef struct tq_codebook_t {
+    int32_t levels;
+    const float* centroids;
+    const float* thresholds;
+} tq_codebook_t;
+
+/* A rotation.  dim: length of the rotated vectors.  block: Hadamard order, a
+ * power of two with 1 <= block <= 8192 dividing dim.  signs: device
+ * int8[dim] holding +1 or -1. */
+typedef struct tq_rotation_t {
+    int32_t dim;
+    int32_t block;
+    const int8_t* signs;
+} tq_rotation_t;
+
+/* A bank of `experts` quantized matrices of shape [rows, cols], stored
+ * rotated along cols.  Expert e, row n starts at codes + e*expert_stride_words
+ * + n*row_stride_words and at scales + e*expert_stride_scales + n*(cols/group).
+ * row_stride_words: >= tq_row_words(levels, cols) and a multiple of 4 (rows
+ * start 16-byte aligned).  expert_stride_words: >= rows*row_stride_words,
+ * multiple of 4.  expert_stride_scales >= rows*cols/group.  group: 16, 32, 64
+ * or 128, dividing cols.  A dense (non-MoE) matrix is a bank with experts = 1. */
+typedef struct tq_qweight_t {
+    const uint32_t* codes;
+    const uint16_t* scales;
+    int32_t experts;
+    int32_t rows;
+    int32_t cols;
+    int32_t group;
+    int64_t row_stride_words;
+    int64_t expert_stride_words;
+    int64_t expert_stride_scales;
+    tq_codebook_t cb;
+} tq_qweight_t;
+
+/* ------------------------------------------------------------------ host helpers */
+
+/* Human-readable name of a status.  Never NULL. */
+const char* tq_status_string(tq_status s);
+
+/* Codes per 32-bit word for a codebook size ("The ternary tier": 3 entries =>
+ * 20 trits; "Quantizing a weight", step Pack: 2^b entries => 32/b codes).
+ * Returns 0 for an unsupported size. */
+int32_t tq_codes_per_word(int32_t levels);
+
+/* Words holding one row of `cols` codes (ceil(cols / codes_per_word)); 0 if invalid. */
+int64_t tq_row_words(int32_t levels, int32_t cols);
+
+/* tq_row_words rounded up to a multiple of 4 (the padded row stride). */
+int64_t tq_row_stride_words(int32_t levels, int32_t cols);
+
+/* Gaussian Lloyd-Max codebook, computed on the host in fp64.
+ * "How it works", "Quantizing a weight, with no data", step "Snap to a
+ * codebook": the error-minimising quantizer for a Gaussian, a fixed constant
+ * per bit width; "The ternary tier": the three-level book {-c, 0, +c}.
+ * levels: 2, 3, 4, 8, 16 or 256.  centroids: host double[levels];
+ * thresholds: host double[levels-1] (midpoints).  Both ascending and exactly
+ * symmetric about 0.  Returns TQ_ERR_INVALID for other sizes or NULL output. */
+tq_status tq_codebook(int32_t levels, double* centroids, double* thresholds);
+
+/* Rotation sign vector from a seed, on the host.
+ * "How it works", "Configuration that converter and loader share": the
+ * rotation's seed is recorded with the model; for a Hadamard layer the
+ * rotation is a dim-length +-1 vector.  signs[i] = -1 if the top bit of the
+ * i-th SplitMix64 output (Steele, Lea & Flood 2014) for `seed` is set, else +1.
+ * signs: host int8[dim]. */
+tq_status tq_rotation_signs(uint64_t seed, int32_t dim, int8_t* signs);
+
+/* ------------------------------------------------------------------ device entry points */
+
+/* x_rot = R x for `rows` vectors.
+ * "How it works", "Running a quantized layer": the layer rotates its input
+ * (R orthonormal) instead of un-rotating the weights.
+ * x: device [rows, rot->dim] of dtype xdt (f32, bf16 or f16).  x_rot: device
+ * [rows, rot->dim] of dtype ydt (f32, bf16 or f16), may not alias x. */
+tq_status tq_rotate(const tq_rotation_t* rot, const void* x, tq_dtype xdt, int64_t rows,
+                    void* x_rot, tq_dtype ydt, void* stream);
+
+/* Fused encode of weight rows: rotate, per-group RMS, snap, pack.
+ * "How it works", "Quantizing a weight, with no data" (all four steps).
+ * W: device [rows, cols] of dtype wdt (f32 or bf16); rot->dim == cols.
+ * Each group of `group` rotated values is divided by its RMS
+ * sqrt(sum v^2 / group) computed in fp32 (a zero group gives u = 0); the
+ * stored scale is that RMS rounded to fp16 (nearest even).  The code of u is
+ * the number of thresholds strictly below u (fp32 compare).
+ * codes: device uint32 [rows, row_stride_words] (padding written as zero);
+ * scales: device fp16 [rows, cols/group].  cb->levels: 3, 4, 8 or 16. */
+tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int32_t cols, int32_t group,
+                      const tq_rotation_t* rot, const tq_codebook_t* cb,
+                      uint32_t* codes, uint16_t* scales, int64_t row_stride_words, void* stream);
+
+/* Dense quantized matvec, codes decoded inline: y[t, n] = sum_k W_rot[n, k] x_rot[t, k]
+ * with W_rot[n, k] = fp16 scale[n, k/group] * centroid[code[n, k]] of expert 0.
+ * "How it works", "Running a quantized layer": fused kernels decode the packed
+ * codes inline, so the full-precision weights never exist.
+ * x_rot: device f32 [T, cols] (already rotated).  y: device [T, rows] of ydt
+ * (f32 or bf16).  T >= 1.  cb->levels: 3, 4, 8 or 16. */
+tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T, void* y, tq_dtype ydt, void* stream);
+
+/* MoE decode: every routed expert reads the shared input of its token.
+ * "How it works", "Running a quantized layer", row "Decoding one token"
+ * (polar_gather_qmv).  y[t, j, :] = W_{ids[t, j]} x_rot[t].
+ * x_rot: device f32 [T, cols].  ids: device int32 [T, k].  y: device
+ * [T, k, rows] of ydt (f32 or bf16).  Out-of-range ids zero their row of y
+ * and set TQ_DEVERR_BAD_ID in *err. */
+tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
+                        void* y, tq_dtype ydt, uint32_t* err, void* stream);
+
+/* MoE with a different input for each (expert, input) pair.
+ * "How it works", row "Prefill with a different input per expert"
+ * (polar_multi_gather_qmv).  y[p, :] = W_{ids[p]} x_rot[p].
+ * x_rot: device f32 [P, cols].  ids: device int32 [P].  y: device [P, rows]
+ * of ydt (f32 or bf16). */
+tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
+                              void* y, tq_dtype ydt, uint32_t* err, void* stream);
+
+/* Router: top-k experts per token, softmax weights, expert-sorted pair order.
+ * "Running a 1T-Parameter Model on a Laptop": the router picks the 8 best of
+ * 384 experts per token; "How it works", row "A large batch sorted by expert".
+ * logits: device f32 [T, E] (E <= 1024, k <= 32, k <= E).  Ties go to the
+ * lower expert id; ids[t, :] is in descending logit order.  probs: softmax over
+ * the k selected logits.  Pairs f = t*k + j are sorted by (expert, f):
+ * perm[i] = pair at sorted position i; pair_pos[f] = sorted position of pair f;
+ * offsets[e] = first sorted position of expert e, offsets[E] = T*k.
+ * ids, perm, pair_pos: device int32 [T*k]; probs: device f32 [T*k];
+ * offsets: device int32 [E+1].  ws: device scratch of at least
+ * tq_route_workspace_bytes(E) bytes (contents need not be initialised). */
+tq_status tq_moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* probs,
+                       int32_t* perm, int32_t* pair_pos, int32_t* offsets, void* ws, size_t ws_bytes,
+                       void* stream);
+size_t tq_route_workspace_bytes(int32_t E);
+
+/* SwiGLU between an expert's gate/up and down projections, followed by the
+ * rotation of the intermediate (the down projection consumes R h).
+ * gate_up: device f32 [P, 2*inter], gate in columns [0, inter), up in
+ * [inter, 2*inter).  h_rot[p] = R (silu(gate) * up), silu(g) = g / (1 + e^-g).
+ * rot->dim == inter.  h_rot: device [P, inter] of ydt (f32, bf16 or f16). */
+tq_status tq_swiglu_rotate(const float* gate_up, int64_t P, int32_t inter, const tq_rotation_t* rot,
+                           void* h_rot, tq_dtype ydt, void* stream);
+
+/* Router-weighted sum of the experts' outputs: out[t] = sum_j probs[t*k+j] * y[row(t*k+j)],
+ * row(f) = pair_pos[f] when pair_pos is not NULL (y in expert-sorted order),
+ * else f (y in pair order).  y: device f32 [T*k, H].  out: device [T, H] of
+ * odt (f32 or bf16). */
+tq_status tq_moe_combine(const float* y, const float* probs, const int32_t* pair_pos, int32_t T, int32_t k,
+                         int32_t H, void* out, tq_dtype odt, void* stream);
+
+/* MoE prefill: expert-sorted batched gather-GEMM on the tensor cores.
+ * "How it works", row "A large batch sorted by expert" (polar_gather_qmm).
+ * For sorted position i with expert e (offsets[e] <= i < offsets[e+1]):
+ *   y[i, :] = W_e x_src(i),  src(i) = perm[i] / k  (per_pair_input == 0: rows of
+ *   x are tokens) or src(i) = i (per_pair_input != 0: rows of x are the
+ *   sorted pairs' own inputs).
+ * Codes are decoded to the operand type xdt (f16 or bf16) in shared memory and
+ * multiplied with fp32 accumulation.  x: device [T or P, cols] of xdt (already
+ * rotated).  perm: device int32 [P] (ignored when per_pair_input);
+ * offsets: device int32 [experts+1].  y: device [P, rows] of ydt (f32 or
+ * bf16).  ws: device scratch of tq_gather_qmm_workspace_bytes(experts) bytes.
+ * cols must be a multiple of 64, rows a multiple of 128. */
+tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtype xdt, const int32_t* perm,
+                        const int32_t* offsets, int32_t P, int32_t k, int32_t per_pair_input,
+                        void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
+size_t tq_gather_qmm_workspace_bytes(int32_t experts);
+
+/* Dequantize selected experts to dense rotated-domain weights, for a regular matmul.
+ * "How it works", row "Anything else" (polar_dequant_experts).
+ * out[i, n, c] = fp16 scale * centroid of expert ids[i]; out: device
+ * [n_ids, rows, cols] of odt (f32, bf16 or f16).  The caller multiplies by the
+ * rotated input. */
+tq_status tq_dequant_experts(const tq_qweight_t* w, const int32_t* ids, int32_t n_ids, void* out, tq_dtype odt,
+                             uint32_t* err, void* stream);
+
+/* KV cache compression of T new tokens at positions [pos, pos+T).
+ * "How it works", "The KV cache": the same rotation and codebook compress the
+ * cache at run time (8-bit keys, 3-bit values recommended);
+ * "Running a 1T-Parameter Model on a Laptop", update_and_fetch: rotate, then
+ * quantize.  Each (token, head) vector of D is rotated by rot (dim = block =
+ * D), split into groups of `group`, scaled by the group RMS and snapped.
+ * k, v: device [T, Hkv, D] of dt (f32 or bf16).  Outputs, for each head h and
+ * position p: kcodes + (h*capacity + p)*kw (kw = tq_row_words(kcb->levels, D)
+ * words), kscales + (h*capacity + p)*(D/group), and the same for v with vw.
+ * D: 128 (one warp per vector).  kcb/vcb levels: 3, 4, 8, 16 or 256. */
+tq_status tq_kv_quantize(const void* k, const void* v, tq_dtype dt, int32_t T, int32_t Hkv, int32_t D,
+                         int64_t pos, int64_t capacity, const tq_rotation_t* rot,
+                         const tq_codebook_t* kcb, const tq_codebook_t* vcb, int32_t group,
+                         uint32_t* kcodes, uint16_t* kscales, uint32_t* vcodes, uint16_t* vscales,
+                         void* stream);
+
+/* One decode step of attention read straight from the compressed cache.
+ * "Running a 1T-Parameter Model on a Laptop", update_and_fetch: the cache is
+ * dequantized and de-rotated and attention softmax(q K^T / sqrt(D)) V runs on
+ * it.  Here the rotation is moved algebraically: q_rot = R q, scores
+ * q_rot . k_rot_hat / sqrt(D), o = R^T sum_t p_t v_rot_hat(t) (one
+ * de-rotation of the output instead of one per cached token).
+ * q: device [Hq, D] of qdt (f32 or bf16); query head h reads kv head
+ * h / (Hq/Hkv).  Cache layout as written by tq_kv_quantize, first ctx
+ * positions.  o: device f32 [Hq, D].  ws: device scratch of
+ * tq_kv_attend_workspace_bytes(Hq, D, ctx) bytes.  D: 128. */
+tq_status tq_kv_attend(const void* q, tq_dtype qdt, int32_t Hq, int32_t Hkv, int32_t D, int64_t ctx,
+                       int64_t capacity, const tq_rotation_t* rot, const tq_codebook_t* kcb, const tq_codebook_t* vcb,
+                       int32_t group, const uint32_t* kcodes, const uint16_t* kscales, const uint32_t* vcodes,
+                       const uint16_t* vscales, float* o, void* ws, size_t ws_bytes, void* stream);
+size_t tq_kv_attend_workspace_bytes(int32_t Hq, int32_t D, int64_t ctx);
+
+/* Waits for `stream`, reads the device error word and clears it.
+ * Returns TQ_OK if it was 0, TQ_ERR_TIMEOUT if TQ_DEVERR_TIMEOUT is set, else
+ * TQ_ERR_DEVICE; *bits (host, may be NULL) receives the word. */
+tq_status tq_check_error(uint32_t* err, uint32_t* bits, void* stream);
+
+/* Exhaustive self-check of the divide-free base-3 digit decoder used by the
+ * ternary kernels: decodes every word in [first, first+count) (count words,
+ * first+count <= 3^20) and compares each digit with plain division.
+ * mismatches: device uint64 counter, incremented per wrong word (caller
+ * zeroes it).  For tests. */
+tq_status tq_selftest_trit_decode(uint32_t first, uint32_t count, unsigned long long* mismatches, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,401 @@
+"""Python binding of libtq.so, the CUDA library of rotated-codebook quantization.
+
+Argument marshalling only: every function here checks shapes, allocates the
+output tensors with torch (device memory), and calls the C entry point of the
+same name on torch's current CUDA stream.  All arithmetic runs in the library's
+kernels.  There is no CPU fallback: if the library cannot be loaded, ``load()``
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtq.so")
+
+TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
+TQ_OK, TQ_ERR_INVALID, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_TIMEOUT, TQ_ERR_DEVICE = range(6)
+TQ_DEVERR_BAD_ID, TQ_DEVERR_TIMEOUT, TQ_DEVERR_BAD_BOOK = 1, 2, 4
+
+_c_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_u32 = ctypes.c_uint32
+_sz = ctypes.c_size_t
+
+
+class tq_codebook_t(ctypes.Structure):
+    _fields_ = [("levels", _i32), ("centroids", _c_p), ("thresholds", _c_p)]
+
+
+class tq_rotation_t(ctypes.Structure):
+    _fields_ = [("dim", _i32), ("block", _i32), ("signs", _c_p)]
+
+
+class tq_qweight_t(ctypes.Structure):
+    _fields_ = [("codes", _c_p), ("scales", _c_p), ("experts", _i32), ("rows", _i32), ("cols", _i32),
+                ("group", _i32), ("row_stride_words", _i64), ("expert_stride_words", _i64),
+                ("expert_stride_scales", _i64), ("cb", tq_codebook_t)]
+
+
+_P = ctypes.POINTER
+# name -> (restype, argtypes), exactly the declarations of include/tq.h
+_SIGS = {
+    "tq_status_string": (ctypes.c_char_p, [_i32]),
+    "tq_codes_per_word": (_i32, [_i32]),
+    "tq_row_words": (_i64, [_i32, _i32]),
+    "tq_row_stride_words": (_i64, [_i32, _i32]),
+    "tq_codebook": (_i32, [_i32, _P(ctypes.c_double), _P(ctypes.c_double)]),
+    "tq_rotation_signs": (_i32, [ctypes.c_uint64, _i32, _P(ctypes.c_int8)]),
+    "tq_rotate": (_i32, [_P(tq_rotation_t), _c_p, _i32, _i64, _c_p, _i32, _c_p]),
+    "tq_quantize": (_i32, [_c_p, _i32, _i64, _i32, _i32, _P(tq_rotation_t), _P(tq_codebook_t), _c_p, _c_p, _i64,
+                           _c_p]),
+    "tq_qmv": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p]),
+    "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p]),
+    "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
+    "tq_moe_route": (_i32, [_c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _sz, _c_p]),
+    "tq_route_workspace_bytes": (_sz, [_i32]),
+    "tq_swiglu_rotate": (_i32, [_c_p, _i64, _i32, _P(tq_rotation_t), _c_p, _i32, _c_p]),
+    "tq_moe_combine": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _i32, _c_p]),
+    "tq_gather_qmm": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _i32, _i32, _i32, _c_p, _i32, _c_p, _sz,
+                             _c_p, _c_p]),
+    "tq_gather_qmm_workspace_bytes": (_sz, [_i32]),
+    "tq_dequant_experts": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
+    "tq_kv_quantize": (_i32, [_c_p, _c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t),
+                              _P(tq_codebook_t), _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "tq_kv_attend": (_i32, [_c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t), _P(tq_codebook_t),
+                            _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _sz, _c_p]),
+    "tq_kv_attend_workspace_bytes": (_sz, [_i32, _i32, _i64]),
+    "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
+    "tq_selftest_trit_decode": (_i32, [_u32, _u32, _c_p, _c_p]),
+}
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libtq.so (raises if it is missing) and declare every entry point."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libtq.so not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class TQError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != TQ_OK:
+        raise TQError(f"{what}: {load().tq_status_string(status).decode()} ({status})")
+
+
+# ---------------------------------------------------------------- torch marshalling
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    return {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16, torch.float16: TQ_F16}[t.dtype]
+
+
+def _torch_dtype(code: int):
+    torch = _torch()
+    return {TQ_F32: torch.float32, TQ_BF16: torch.bfloat16, TQ_F16: torch.float16}[code]
+
+
+def _contig(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+# ---------------------------------------------------------------- host helpers
+
+def codes_per_word(levels: int) -> int:
+    return int(load().tq_codes_per_word(levels))
+
+
+def row_words(levels: int, cols: int) -> int:
+    return int(load().tq_row_words(levels, cols))
+
+
+def row_stride_words(levels: int, cols: int) -> int:
+    return int(load().tq_row_stride_words(levels, cols))
+
+
+def codebook(levels: int):
+    """Host fp64 Gaussian Lloyd-Max book: (centroids[levels], thresholds[levels-1]) numpy arrays."""
+    c = np.zeros(levels, dtype=np.float64)
+    t = np.zeros(max(levels - 1, 1), dtype=np.float64)
+    _check(load().tq_codebook(levels, c.ctypes.data_as(_P(ctypes.c_double)), t.ctypes.data_as(_P(ctypes.c_double))),
+           "tq_codebook")
+    return c, t[:levels - 1]
+
+
+def rotation_signs(seed: int, dim: int) -> np.ndarray:
+    s = np.zeros(dim, dtype=np.int8)
+    _check(load().tq_rotation_signs(ctypes.c_uint64(seed), dim, s.ctypes.data_as(_P(ctypes.c_int8))),
+           "tq_rotation_signs")
+    return s
+
+
+# ---------------------------------------------------------------- device descriptors
+
+class Codebook:
+    """A codebook on the device: fp32 centroids and thresholds."""
+
+    def __init__(self, levels: int, device="cuda", centroids=None, thresholds=None):
+        torch = _torch()
+        if centroids is None:
+            centroids, thresholds = codebook(levels)
+        self.levels = int(levels)
+        self.centroids = torch.tensor(np.asarray(centroids, np.float32), device=device)
+        self.thresholds = torch.tensor(np.asarray(thresholds, np.float32).reshape(-1), device=device)
+        if self.thresholds.numel() == 0:
+            self.thresholds = torch.zeros(1, dtype=torch.float32, device=device)
+
+    def c(self) -> tq_codebook_t:
+        return tq_codebook_t(self.levels, self.centroids.data_ptr(), self.thresholds.data_ptr())
+
+
+class Rotation:
+    """R = blockdiag(H_block) diag(signs) / sqrt(block) over vectors of length dim."""
+
+    def __init__(self, dim: int, block: int, seed: int | None = None, signs=None, device="cuda"):
+        torch = _torch()
+        if signs is None:
+            signs = rotation_signs(seed, dim)
+        self.dim, self.block = int(dim), int(block)
+        self.signs = torch.tensor(np.asarray(signs, np.int8), device=device)
+
+    def c(self) -> tq_rotation_t:
+        return tq_rotation_t(self.dim, self.block, self.signs.data_ptr())
+
+
+class QWeight:
+    """A bank of quantized matrices [experts, rows, cols] as written by ``quantize``."""
+
+    def __init__(self, codes, scales, experts: int, rows: int, cols: int, group: int, cb: Codebook,
+                 row_stride: int | None = None):
+        self.codes, self.scales, self.cb = codes, scales, cb
+        self.experts, self.rows, self.cols, self.group = int(experts), int(rows), int(cols), int(group)
+        self.row_stride = int(row_stride if row_stride is not None else row_stride_words(cb.levels, cols))
+
+    def c(self) -> tq_qweight_t:
+        esw = self.rows * self.row_stride
+        ess = self.rows * (self.cols // self.group)
+        return tq_qweight_t(self.codes.data_ptr(), self.scales.data_ptr(), self.experts, self.rows, self.cols,
+                            self.group, self.row_stride, esw, ess, self.cb.c())
+
+
+# ---------------------------------------------------------------- device entry points
+
+def rotate(x, rot: Rotation, out_dtype=None):
+    torch = _torch()
+    _contig(x, "x")
+    out = torch.empty(x.shape, dtype=out_dtype or torch.float32, device=x.device)
+    r = rot.c()
+    _check(load().tq_rotate(ctypes.byref(r), _ptr(x), _dt(x), x.numel() // rot.dim, _ptr(out), _dt(out), _stream()),
+           "tq_rotate")
+    return out
+
+
+def quantize(W, group: int, rot: Rotation, cb: Codebook, row_stride: int | None = None):
+    """Encode rows of W [rows, cols] -> (codes uint32 [rows, stride] as int32 storage, scales fp16 bits)."""
+    torch = _torch()
+    _contig(W, "W")
+    rows, cols = W.shape
+    stride = row_stride if row_stride is not None else row_stride_words(cb.levels, cols)
+    codes = torch.empty((rows, stride), dtype=torch.int32, device=W.device)
+    scales = torch.empty((rows, cols // group), dtype=torch.int16, device=W.device)
+    r, b = rot.c(), cb.c()
+    _check(load().tq_quantize(_ptr(W), _dt(W), rows, cols, group, ctypes.byref(r), ctypes.byref(b), _ptr(codes),
+                              _ptr(scales), stride, _stream()), "tq_quantize")
+    return codes, scales
+
+
+def qmv(w: QWeight, x_rot, out_dtype=None):
+    torch = _torch()
+    _contig(x_rot, "x_rot")
+    T = x_rot.shape[0]
+    y = torch.empty((T, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
+    q = w.c()
+    _check(load().tq_qmv(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _dt(y), _stream()), "tq_qmv")
+    return y
+
+
+def gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
+    torch = _torch()
+    _contig(x_rot, "x_rot")
+    _contig(ids, "ids")
+    T, k = ids.shape
+    y = torch.empty((T, k, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
+    q = w.c()
+    _check(load().tq_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), T, k, _ptr(y), _dt(y), _ptr(err), _stream()),
+           "tq_gather_qmv")
+    return y
+
+
+def multi_gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
+    torch = _torch()
+    _contig(x_rot, "x_rot")
+    _contig(ids, "ids")
+    P = ids.shape[0]
+    y = torch.empty((P, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
+    q = w.c()
+    _check(load().tq_multi_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), P, _ptr(y), _dt(y), _ptr(err),
+                                      _stream()), "tq_multi_gather_qmv")
+    return y
+
+
+def moe_route(logits, k: int):
+    """-> ids [T,k] int32, probs [T,k] f32, perm [T*k], pair_pos [T*k], offsets [E+1]."""
+    torch = _torch()
+    _contig(logits, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    probs = torch.empty((T, k), dtype=torch.float32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    nb = int(load().tq_route_workspace_bytes(E))
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    _check(load().tq_moe_route(_ptr(logits), T, E, k, _ptr(ids), _ptr(probs), _ptr(perm), _ptr(pos), _ptr(off),
+                               _ptr(ws), nb, _stream()), "tq_moe_route")
+    return ids, probs, perm, pos, off
+
+
+def swiglu_rotate(gate_up, inter: int, rot: Rotation, out_dtype=None):
+    torch = _torch()
+    _contig(gate_up, "gate_up")
+    P = gate_up.numel() // (2 * inter)
+    out = torch.empty((P, inter), dtype=out_dtype or torch.float32, device=gate_up.device)
+    r = rot.c()
+    _check(load().tq_swiglu_rotate(_ptr(gate_up), P, inter, ctypes.byref(r), _ptr(out), _dt(out), _stream()),
+           "tq_swiglu_rotate")
+    return out
+
+
+def moe_combine(y, probs, k: int, pair_pos=None, out_dtype=None):
+    torch = _torch()
+    _contig(y, "y")
+    H = y.shape[-1]
+    T = probs.numel() // k
+    out = torch.empty((T, H), dtype=out_dtype or torch.float32, device=y.device)
+    _check(load().tq_moe_combine(_ptr(y), _ptr(probs), _ptr(pair_pos), T, k, H, _ptr(out), _dt(out), _stream()),
+           "tq_moe_combine")
+    return out
+
+
+def gather_qmm(w: QWeight, x, perm, offsets, k: int, per_pair_input: bool = False, out_dtype=None, err=None):
+    torch = _torch()
+    _contig(x, "x")
+    P = int(perm.numel()) if not per_pair_input else int(x.shape[0])
+    y = torch.empty((P, w.rows), dtype=out_dtype or torch.float32, device=x.device)
+    nb = int(load().tq_gather_qmm_workspace_bytes(w.experts))
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=x.device)
+    q = w.c()
+    _check(load().tq_gather_qmm(ctypes.byref(q), _ptr(x), _dt(x), _ptr(perm), _ptr(offsets), P, k,
+                                int(per_pair_input), _ptr(y), _dt(y), _ptr(ws), nb, _ptr(err), _stream()),
+           "tq_gather_qmm")
+    return y
+
+
+def dequant_experts(w: QWeight, ids, out_dtype=None, err=None):
+    torch = _torch()
+    _contig(ids, "ids")
+    n = ids.numel()
+    out = torch.empty((n, w.rows, w.cols), dtype=out_dtype or torch.float32, device=ids.device)
+    q = w.c()
+    _check(load().tq_dequant_experts(ctypes.byref(q), _ptr(ids), n, _ptr(out), _dt(out), _ptr(err), _stream()),
+           "tq_dequant_experts")
+    return out
+
+
+class KVCache:
+    """Compressed KV cache: codes and fp16 scales per (kv head, position)."""
+
+    def __init__(self, capacity: int, heads: int, dim: int, group: int, kcb: Codebook, vcb: Codebook,
+                 rot: Rotation, device="cuda"):
+        torch = _torch()
+        self.capacity, self.heads, self.dim, self.group = capacity, heads, dim, group
+        self.kcb, self.vcb, self.rot = kcb, vcb, rot
+        self.kw, self.vw = row_words(kcb.levels, dim), row_words(vcb.levels, dim)
+        self.kcodes = torch.zeros((heads, capacity, self.kw), dtype=torch.int32, device=device)
+        self.vcodes = torch.zeros((heads, capacity, self.vw), dtype=torch.int32, device=device)
+        self.kscales = torch.zeros((heads, capacity, dim // group), dtype=torch.int16, device=device)
+        self.vscales = torch.zeros((heads, capacity, dim // group), dtype=torch.int16, device=device)
+        self.length = 0
+
+
+def kv_quantize(cache: KVCache, k, v, pos: int | None = None):
+    _contig(k, "k")
+    _contig(v, "v")
+    T = k.shape[0]
+    pos = cache.length if pos is None else pos
+    r, kb, vb = cache.rot.c(), cache.kcb.c(), cache.vcb.c()
+    _check(load().tq_kv_quantize(_ptr(k), _ptr(v), _dt(k), T, cache.heads, cache.dim, pos, cache.capacity,
+                                 ctypes.byref(r), ctypes.byref(kb), ctypes.byref(vb), cache.group, _ptr(cache.kcodes),
+                                 _ptr(cache.kscales), _ptr(cache.vcodes), _ptr(cache.vscales), _stream()),
+           "tq_kv_quantize")
+    cache.length = max(cache.length, pos + T)
+
+
+def kv_attend(cache: KVCache, q, ctx: int | None = None, ws=None):
+    torch = _torch()
+    _contig(q, "q")
+    Hq = q.shape[0]
+    ctx = cache.length if ctx is None else ctx
+    o = torch.empty((Hq, cache.dim), dtype=torch.float32, device=q.device)
+    nb = int(load().tq_kv_attend_workspace_bytes(Hq, cache.dim, ctx))
+    if ws is None:
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
+    r, kb, vb = cache.rot.c(), cache.kcb.c(), cache.vcb.c()
+    _check(load().tq_kv_attend(_ptr(q), _dt(q), Hq, cache.heads, cache.dim, ctx, cache.capacity, ctypes.byref(r),
+                               ctypes.byref(kb), ctypes.byref(vb), cache.group, _ptr(cache.kcodes),
+                               _ptr(cache.kscales), _ptr(cache.vcodes), _ptr(cache.vscales), _ptr(o), _ptr(ws),
+                               ws.numel(), _stream()), "tq_kv_attend")
+    return o
+
+
+def check_error(err) -> int:
+    """Synchronises, returns the device error bits and clears them."""
+    bits = _u32(0)
+    st = load().tq_check_error(_ptr(err), ctypes.byref(bits), _stream())
+    if st not in (TQ_OK, TQ_ERR_TIMEOUT, TQ_ERR_DEVICE):
+        _check(st, "tq_check_error")
+    return int(bits.value)
+
+
+def selftest_trit_decode(first: int = 0, count: int = 3 ** 20) -> int:
+    torch = _torch()
+    m = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(load().tq_selftest_trit_decode(first, count, _ptr(m), _stream()), "tq_selftest_trit_decode")
+    return int(m.item())

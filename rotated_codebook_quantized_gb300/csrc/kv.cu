@@ -1,0 +1,252 @@
+// One decode step of attention read straight from the compressed KV cache:
+// tq_kv_attend.
+//
+// "Running a 1T-Parameter Model on a Laptop", update_and_fetch: the cache is
+// dequantized and de-rotated, then softmax(q K^T / sqrt(D)) V.  Rotation is
+// orthonormal, so q . k = (R q) . (R k): the query is rotated once, scores use
+// the rotated, dequantized keys as stored, and the weighted sum of rotated
+// values is de-rotated once at the end.  "How it works", "The KV cache": the
+// same rotation and codebook as the weights (8-bit keys, 3-bit values).
+//
+// Split-context (flash-decoding) layout: CTA (kv head, chunk) scores its chunk
+// of tokens for the Hq/Hkv query heads that share the kv head, keeps the
+// chunk's max and sum, and writes an unnormalised partial output; a second
+// kernel merges the chunks and de-rotates.
+#include <math.h>
+
+#include "common.cuh"
+
+using namespace tq;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kChunk = 1024;   // tokens per CTA
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kMaxGQ = 8;      // query heads per kv head
+
+template <int LEVELS>
+struct KvFmt {
+    static constexpr int kBits = LEVELS == 256 ? 8 : (LEVELS == 16 ? 4 : (LEVELS == 8 ? 3 : 2));
+    static constexpr int kCW = LEVELS == 8 ? 10 : 32 / kBits;
+    static constexpr int kWords = (kD + kCW - 1) / kCW;
+};
+
+template <int KL, int VL, int GQ>
+__global__ void __launch_bounds__(kThreads) kv_partial_kernel(
+    const void* __restrict__ q, int qdt, int Hkv, int64_t ctx, int64_t capacity, const int8_t* __restrict__ signs,
+    const float* __restrict__ kcent, const float* __restrict__ vcent, int group,
+    const uint32_t* __restrict__ kcodes, const uint16_t* __restrict__ kscales, const uint32_t* __restrict__ vcodes,
+    const uint16_t* __restrict__ vscales, float* __restrict__ part, int nsplit) {
+    using KF = KvFmt<KL>;
+    using VF = KvFmt<VL>;
+    __shared__ __align__(16) float qs[GQ][kD];  // rotated query / sqrt(D)
+    __shared__ float klut[KL];
+    __shared__ float vlut[VL];
+    __shared__ float sc[GQ][kChunk];           // scores, then probabilities
+    __shared__ float obuf[GQ][kD];             // sum over warps of the weighted values
+    __shared__ float stat[GQ][2];
+
+    const int h = blockIdx.x, split = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)split * kChunk;
+    const int n = (int)min((int64_t)kChunk, ctx - t0);
+    const int ng = kD / group;
+
+    for (int i = threadIdx.x; i < KL; i += kThreads) klut[i] = kcent[i];
+    for (int i = threadIdx.x; i < GQ * kD; i += kThreads) (&obuf[0][0])[i] = 0.f;
+    for (int i = threadIdx.x; i < VL; i += kThreads) vlut[i] = vcent[i];
+    // q_rot = H diag(s) q / sqrt(D), and the 1/sqrt(D) of the scores folded in.
+    for (int g = warp; g < GQ; g += kThreads / 32) {
+        const int hq = h * GQ + g;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = load_as_float(q, (int64_t)hq * kD + lane * 4 + i, qdt) * (float)signs[lane * 4 + i];
+        fwht_warp128(v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[g][lane * 4 + i] = v[i] * (1.0f / 128.0f);  // (1/sqrt(128))^2
+    }
+    __syncthreads();
+
+    // Scores: one thread per token; the query is read with broadcast loads.
+    const uint32_t* kbase = kcodes + ((int64_t)h * capacity + t0) * KF::kWords;
+    const uint16_t* ksbase = kscales + ((int64_t)h * capacity + t0) * ng;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t* kr = kbase + (int64_t)i * KF::kWords;
+        const uint16_t* sr = ksbase + (int64_t)i * ng;
+        float acc[GQ], tot[GQ];
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) tot[g] = 0.f;
+        for (int g0 = 0; g0 < ng; ++g0) {
+#pragma unroll
+            for (int g = 0; g < GQ; ++g) acc[g] = 0.f;
+            for (int d = g0 * group; d < (g0 + 1) * group; ++d) {
+                const uint32_t w = kr[d / KF::kCW];
+                const uint32_t c = (w >> (KF::kBits * (d % KF::kCW))) & (KL - 1);
+                const float cv = klut[c];
+#pragma unroll
+                for (int g = 0; g < GQ; ++g) acc[g] = fmaf(cv, qs[g][d], acc[g]);
+            }
+            const float s = half_bits_to_float(sr[g0]);
+#pragma unroll
+            for (int g = 0; g < GQ; ++g) tot[g] = fmaf(s, acc[g], tot[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) sc[g][i] = tot[g];
+    }
+    __syncthreads();
+
+    // Chunk max and sum per head (warp g handles head g).
+    for (int g = warp; g < GQ; g += kThreads / 32) {
+        float m = -INFINITY;
+        for (int i = lane; i < n; i += 32) m = fmaxf(m, sc[g][i]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        float l = 0.f;
+        for (int i = lane; i < n; i += 32) {
+            const float p = expf(sc[g][i] - m);
+            sc[g][i] = p;
+            l += p;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+        if (lane == 0) {
+            stat[g][0] = m;
+            stat[g][1] = l;
+        }
+    }
+    __syncthreads();
+
+    // Weighted sum of rotated values: warp per token, lane owns dims 4l..4l+3.
+    float o[GQ][4];
+#pragma unroll
+    for (int g = 0; g < GQ; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[g][j] = 0.f;
+    const uint32_t* vbase = vcodes + ((int64_t)h * capacity + t0) * VF::kWords;
+    const uint16_t* vsbase = vscales + ((int64_t)h * capacity + t0) * ng;
+    const int gl = (lane * 4) / group;  // the lane's four dims share one group (group >= 4)
+    for (int i = warp; i < n; i += kThreads / 32) {
+        const uint32_t* vr = vbase + (int64_t)i * VF::kWords;
+        const float s = half_bits_to_float(vsbase[(int64_t)i * ng + gl]);
+        float vv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int d = lane * 4 + j;
+            const uint32_t w = vr[d / VF::kCW];
+            vv[j] = s * vlut[(w >> (VF::kBits * (d % VF::kCW))) & (VL - 1)];
+        }
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) {
+            const float p = sc[g][i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g][j] = fmaf(p, vv[j], o[g][j]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < GQ; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) atomicAdd(&obuf[g][lane * 4 + j], o[g][j]);
+    __syncthreads();
+    // part[(split * Hq + hq) * (D + 2)] = {m, l, o[0..D)}
+    for (int idx = threadIdx.x; idx < GQ * kD; idx += kThreads) {
+        const int g = idx / kD, d = idx % kD;
+        const float sum = obuf[g][d];
+        const int hq = h * GQ + g;
+        float* dst = part + ((int64_t)split * Hkv * GQ + hq) * (kD + 2);
+        dst[2 + d] = sum;
+        if (d == 0) {
+            dst[0] = stat[g][0];
+            dst[1] = stat[g][1];
+        }
+    }
+}
+
+// Merge the chunks of one query head and de-rotate: o = diag(s) H o_rot / sqrt(D).
+__global__ void __launch_bounds__(32) kv_merge_kernel(const float* __restrict__ part, int Hq, int nsplit,
+                                                      const int8_t* __restrict__ signs, float* __restrict__ out) {
+    const int hq = blockIdx.x, lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part[((int64_t)s * Hq + hq) * (kD + 2)]);
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < nsplit; ++s) {
+        const float* src = part + ((int64_t)s * Hq + hq) * (kD + 2);
+        const float f = expf(src[0] - M);
+        L = fmaf(f, src[1], L);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = fmaf(f, src[2 + lane * 4 + j], acc[j]);
+    }
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = acc[j] / L;
+    fwht_warp128(v);
+    const float r = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[(int64_t)hq * kD + lane * 4 + j] = v[j] * r * (float)signs[lane * 4 + j];
+}
+
+template <int KL, int VL>
+tq_status launch_kv(int gq, dim3 grid, cudaStream_t st, const void* q, int qdt, int Hkv, int64_t ctx, int64_t capacity,
+                    const int8_t* signs, const float* kc, const float* vc, int group, const uint32_t* kcodes,
+                    const uint16_t* kscales, const uint32_t* vcodes, const uint16_t* vscales, float* part, int nsplit) {
+#define TQ_KV_GQ(G)                                                                                                \
+    case G:                                                                                                        \
+        kv_partial_kernel<KL, VL, G><<<grid, kThreads, 0, st>>>(q, qdt, Hkv, ctx, capacity, signs, kc, vc, group,  \
+                                                                kcodes, kscales, vcodes, vscales, part, nsplit);   \
+        break;
+    switch (gq) {
+        TQ_KV_GQ(1)
+        TQ_KV_GQ(2)
+        TQ_KV_GQ(4)
+        TQ_KV_GQ(8)
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+#undef TQ_KV_GQ
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" size_t tq_kv_attend_workspace_bytes(int32_t Hq, int32_t D, int64_t ctx) {
+    if (Hq <= 0 || D <= 0 || ctx <= 0) return 0;
+    const int64_t nsplit = (ctx + kChunk - 1) / kChunk;
+    return (size_t)nsplit * Hq * (D + 2) * sizeof(float);
+}
+
+extern "C" tq_status tq_kv_attend(const void* q, tq_dtype qdt, int32_t Hq, int32_t Hkv, int32_t D, int64_t ctx,
+                                  int64_t capacity, const tq_rotation_t* rot, const tq_codebook_t* kcb,
+                                  const tq_codebook_t* vcb, int32_t group, const uint32_t* kcodes,
+                                  const uint16_t* kscales, const uint32_t* vcodes, const uint16_t* vscales, float* o,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    if (D != kD) return TQ_ERR_UNSUPPORTED;
+    if (!rot || !rot->signs || rot->dim != D || rot->block != D) return TQ_ERR_INVALID;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || ctx <= 0 || ctx > capacity) return TQ_ERR_INVALID;
+    if (!(group == 16 || group == 32 || group == 64 || group == 128)) return TQ_ERR_INVALID;
+    if (!kcb || !vcb || !kcb->centroids || !vcb->centroids) return TQ_ERR_INVALID;
+    if (qdt != TQ_F32 && qdt != TQ_BF16) return TQ_ERR_INVALID;
+    if (!q || !kcodes || !kscales || !vcodes || !vscales || !o || !ws) return TQ_ERR_INVALID;
+    if (ws_bytes < tq_kv_attend_workspace_bytes(Hq, D, ctx)) return TQ_ERR_INVALID;
+    const int gq = Hq / Hkv;
+    if (gq > kMaxGQ || (gq & (gq - 1))) return TQ_ERR_UNSUPPORTED;
+    const int64_t nsplit = (ctx + kChunk - 1) / kChunk;
+    if (nsplit > 65535 || Hkv > 65535) return TQ_ERR_UNSUPPORTED;
+    cudaStream_t st = as_stream(stream);
+    float* part = reinterpret_cast<float*>(ws);
+    const dim3 grid(Hkv, (unsigned)nsplit);
+    tq_status s;
+    const int kl = kcb->levels, vl = vcb->levels;
+    if (kl == 256 && vl == 8)
+        s = launch_kv<256, 8>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids, vcb->centroids,
+                              group, kcodes, kscales, vcodes, vscales, part, (int)nsplit);
+    else if (kl == 16 && vl == 16)
+        s = launch_kv<16, 16>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids, vcb->centroids,
+                              group, kcodes, kscales, vcodes, vscales, part, (int)nsplit);
+    else if (kl == 256 && vl == 16)
+        s = launch_kv<256, 16>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids, vcb->centroids,
+                               group, kcodes, kscales, vcodes, vscales, part, (int)nsplit);
+    else
+        return TQ_ERR_UNSUPPORTED;
+    if (s != TQ_OK) return s;
+    kv_merge_kernel<<<Hq, 32, 0, st>>>(part, Hq, (int)nsplit, rot->signs, o);
+    return launch_status();
+}

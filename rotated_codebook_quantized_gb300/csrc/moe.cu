@@ -1,0 +1,168 @@
+// Mixture-of-Experts glue: tq_moe_route (top-k, softmax, expert-sorted pair
+// order) and tq_moe_combine (router-weighted sum of expert outputs).
+//
+// "Running a 1T-Parameter Model on a Laptop": a router picks 8 of 384 experts
+// per token and their outputs are combined; "How it works", row "A large batch
+// sorted by expert" (the order polar_gather_qmm consumes).
+#include <math.h>
+
+#include "common.cuh"
+
+using namespace tq;
+
+namespace {
+
+constexpr int kMaxK = 32;
+
+// One warp per token: k rounds of an arg-max over the not-yet-taken experts
+// (ties to the lower id), then a softmax over the k chosen logits.
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ probs,
+                                                         int32_t* __restrict__ counts) {
+    extern __shared__ uint8_t taken_all[];  // [warps][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (t >= T) return;
+    uint8_t* taken = taken_all + warp * E;
+    for (int i = lane; i < E; i += 32) taken[i] = 0;
+    __syncwarp();
+    const float* row = logits + (int64_t)t * E;
+    float chosen_v = 0.f;  // lane j keeps the j-th chosen logit
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = lane; i < E; i += 32) {
+            if (taken[i]) continue;
+            const float v = row[i];
+            if (v > bv || (v == bv && i < bi) || bi == 0x7fffffff) {
+                bv = v;
+                bi = i;
+            }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, m);
+            const int oi = __shfl_xor_sync(kFull, bi, m);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            taken[bi] = 1;
+            ids[(int64_t)t * k + r] = bi;
+            atomicAdd(counts + bi, 1);
+        }
+        if (lane == r) chosen_v = bv;
+        __syncwarp();
+    }
+    // softmax over the k chosen logits; the first is the largest
+    const float mx = __shfl_sync(kFull, chosen_v, 0);
+    const float ex = lane < k ? expf(chosen_v - mx) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(kFull, sum, m);
+    if (lane < k) probs[(int64_t)t * k + lane] = ex / sum;
+}
+
+// offsets[e] = sum of counts below e (one CTA, E <= 1024).
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ counts, int E,
+                                                          int32_t* __restrict__ offsets) {
+    __shared__ int32_t s[1024];
+    const int i = threadIdx.x;
+    s[i] = i < E ? counts[i] : 0;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {  // inclusive Hillis-Steele scan
+        const int v = i >= d ? s[i - d] : 0;
+        __syncthreads();
+        s[i] += v;
+        __syncthreads();
+    }
+    if (i < E) offsets[i + 1] = s[i];
+    if (i == 0) offsets[0] = 0;
+}
+
+// One CTA per expert: walk all pairs in order and compact those routed to it
+// (a stable counting sort: pairs keep their flat order within an expert).
+__global__ void __launch_bounds__(256) route_compact_kernel(const int32_t* __restrict__ ids, int P,
+                                                            const int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos) {
+    __shared__ int warp_tot[8];
+    __shared__ int base_s;
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    if (threadIdx.x == 0) base_s = offsets[e];
+    __syncthreads();
+    for (int f0 = 0; f0 < P; f0 += blockDim.x) {
+        const int f = f0 + threadIdx.x;
+        const bool hit = f < P && ids[f] == e;
+        const unsigned bal = __ballot_sync(kFull, hit);
+        if (lane == 0) warp_tot[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < nwarps; ++w) {
+            before += w < warp ? warp_tot[w] : 0;
+            total += warp_tot[w];
+        }
+        if (hit) {
+            const int pos = base_s + before + __popc(bal & ((1u << lane) - 1u));
+            perm[pos] = f;
+            if (pair_pos) pair_pos[f] = pos;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) base_s += total;
+        __syncthreads();
+    }
+}
+
+__global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ probs,
+                               const int32_t* __restrict__ pair_pos, int k, int H, void* out, int odt) {
+    const int t = blockIdx.y;
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= H) return;
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const int64_t f = (int64_t)t * k + j;
+        const int64_t r = pair_pos ? pair_pos[f] : f;
+        acc = fmaf(probs[f], y[r * H + n], acc);
+    }
+    store_from_float(out, (int64_t)t * H + n, odt, acc);
+}
+
+}  // namespace
+
+extern "C" size_t tq_route_workspace_bytes(int32_t E) { return E > 0 ? ((size_t)E * 4 + 255) / 256 * 256 : 0; }
+
+extern "C" tq_status tq_moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* probs,
+                                  int32_t* perm, int32_t* pair_pos, int32_t* offsets, void* ws, size_t ws_bytes,
+                                  void* stream) {
+    if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > kMaxK || k > E) return TQ_ERR_INVALID;
+    if ((int64_t)T * k > 0x7fffffffll) return TQ_ERR_INVALID;
+    if (!offsets || !ws || ws_bytes < tq_route_workspace_bytes(E)) return TQ_ERR_INVALID;
+    if (T > 0 && (!logits || !ids || !probs || !perm)) return TQ_ERR_INVALID;
+    cudaStream_t st = as_stream(stream);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws);
+    if (cudaMemsetAsync(counts, 0, (size_t)E * 4, st) != cudaSuccess) return TQ_ERR_CUDA;
+    if (T > 0) {
+        const int warps = 8;
+        const size_t smem = (size_t)warps * E;
+        route_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, st>>>(logits, T, E, k, ids, probs, counts);
+        tq_status s = launch_status();
+        if (s != TQ_OK) return s;
+    }
+    route_scan_kernel<<<1, 1024, 0, st>>>(counts, E, offsets);
+    tq_status s = launch_status();
+    if (s != TQ_OK || T == 0) return s;
+    route_compact_kernel<<<E, 256, 0, st>>>(ids, T * k, offsets, perm, pair_pos);
+    return launch_status();
+}
+
+extern "C" tq_status tq_moe_combine(const float* y, const float* probs, const int32_t* pair_pos, int32_t T, int32_t k,
+                                    int32_t H, void* out, tq_dtype odt, void* stream) {
+    if (T < 0 || k <= 0 || H <= 0 || !(odt == TQ_F32 || odt == TQ_BF16)) return TQ_ERR_INVALID;
+    if (T == 0) return TQ_OK;
+    if (!y || !probs || !out || T > 65535) return TQ_ERR_INVALID;
+    combine_kernel<<<dim3((H + 255) / 256, T), 256, 0, as_stream(stream)>>>(y, probs, pair_pos, k, H, out, odt);
+    return launch_status();
+}

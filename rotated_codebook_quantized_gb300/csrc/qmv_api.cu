@@ -1,0 +1,202 @@
+// C ABI of the inline-decode matvec family and of the expert dequantizer.
+//
+// "How it works", "Running a quantized layer": polar_gather_qmv (one token,
+// every routed expert reads the shared input), polar_multi_gather_qmv (a
+// different input per expert), the dense quantized layer, and
+// polar_dequant_experts ("anything else": decode, then a regular matmul).
+#include "qmv_impl.cuh"
+
+using namespace tq;
+
+namespace {
+
+int gcd_i(int a, int b) { return b ? gcd_i(b, a % b) : a; }
+
+// Padded x length per vector in the kernel's shared memory (mirrors QFmt).
+int host_kpad(int levels, int group, int cols) {
+    const int cw = host_codes_per_word(levels);
+    const int uc = cw / gcd_i(cw, group) * group;
+    const int uw = uc / cw;
+    const int s = uw >= 16 ? 1 : 16 / uw;
+    const int units = (cols + uc - 1) / uc;
+    const int nsteps = (units + s - 1) / s;
+    return nsteps * s * uc;
+}
+
+tq_status check_qweight(const tq_qweight_t* w) {
+    if (!w || !w->codes || !w->scales || !w->cb.centroids) return TQ_ERR_INVALID;
+    const int L = w->cb.levels;
+    if (host_codes_per_word(L) == 0) return TQ_ERR_INVALID;
+    if (w->experts <= 0 || w->rows <= 0 || w->cols <= 0) return TQ_ERR_INVALID;
+    if (!(w->group == 16 || w->group == 32 || w->group == 64 || w->group == 128) || w->cols % w->group)
+        return TQ_ERR_INVALID;
+    if (w->row_stride_words < tq_row_words(L, w->cols) || w->row_stride_words % 4) return TQ_ERR_INVALID;
+    if (w->experts > 1 && (w->expert_stride_words < (int64_t)w->rows * w->row_stride_words ||
+                           w->expert_stride_words % 4 ||
+                           w->expert_stride_scales < (int64_t)w->rows * (w->cols / w->group)))
+        return TQ_ERR_INVALID;
+    if (!aligned(w->codes, 16)) return TQ_ERR_INVALID;
+    return TQ_OK;
+}
+
+bool ydt_ok(int d) { return d == TQ_F32 || d == TQ_BF16; }
+
+QmvParams make_params(const tq_qweight_t* w, const float* x, void* y, tq_dtype ydt, uint32_t* err) {
+    QmvParams p{};
+    p.codes = w->codes;
+    p.scales = w->scales;
+    p.row_stride = w->row_stride_words;
+    p.expert_stride_w = w->experts > 1 ? w->expert_stride_words : 0;
+    p.expert_stride_s = w->experts > 1 ? w->expert_stride_scales : 0;
+    p.rows = w->rows;
+    p.cols = w->cols;
+    p.ngroups = w->cols / w->group;
+    p.experts = w->experts;
+    p.centroids = w->cb.centroids;
+    p.levels = w->cb.levels;
+    p.x = x;
+    p.y = y;
+    p.ydt = ydt;
+    p.err = err;
+    return p;
+}
+
+tq_status run(const QmvParams& p, int group, int nv, int n_items, cudaStream_t st) {
+#define TQ_QMV_G(L)                                                     \
+    switch (group) {                                                    \
+        case 16: return qmv_run_l##L##_g16(p, nv, n_items, st);         \
+        case 32: return qmv_run_l##L##_g32(p, nv, n_items, st);         \
+        case 64: return qmv_run_l##L##_g64(p, nv, n_items, st);         \
+        case 128: return qmv_run_l##L##_g128(p, nv, n_items, st);       \
+        default: return TQ_ERR_UNSUPPORTED;                             \
+    }
+    switch (p.levels) {
+        case 3: TQ_QMV_G(3)
+        case 4: TQ_QMV_G(4)
+        case 8: TQ_QMV_G(8)
+        case 16: TQ_QMV_G(16)
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+#undef TQ_QMV_G
+}
+
+// Largest vector batch (1, 2 or 4, at most `want`) whose inputs fit the shared-memory budget.
+int pick_nv(int want, int kpad) {
+    int nv = 1;
+    while (nv * 2 <= want && nv * 2 <= 4 && (size_t)(nv * 2) * kpad * 4 <= 160 * 1024) nv *= 2;
+    return nv;
+}
+
+}  // namespace
+
+extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T, void* y, tq_dtype ydt, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (T < 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
+    if (T == 0) return TQ_OK;
+    if (!x_rot || !y) return TQ_ERR_INVALID;
+    if (w->cb.levels == 2 || w->cb.levels == 256) return TQ_ERR_UNSUPPORTED;
+    QmvParams p = make_params(w, x_rot, y, ydt, nullptr);
+    p.mode = kModeDense;
+    p.T = T;
+    const int nv = pick_nv(T, host_kpad(w->cb.levels, w->group, w->cols));
+    return run(p, w->group, nv, (T + nv - 1) / nv, as_stream(stream));
+}
+
+extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
+                                   void* y, tq_dtype ydt, uint32_t* err, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (T < 0 || k <= 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
+    if (T == 0) return TQ_OK;
+    if (!x_rot || !ids || !y) return TQ_ERR_INVALID;
+    if (w->cb.levels == 2 || w->cb.levels == 256) return TQ_ERR_UNSUPPORTED;
+    if ((int64_t)T * k > 0x7fffffffll) return TQ_ERR_INVALID;
+    QmvParams p = make_params(w, x_rot, y, ydt, err);
+    p.mode = kModeGather;
+    p.ids = ids;
+    p.k = k;
+    return run(p, w->group, 1, T * k, as_stream(stream));
+}
+
+extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
+                                         void* y, tq_dtype ydt, uint32_t* err, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (P < 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
+    if (P == 0) return TQ_OK;
+    if (!x_rot || !ids || !y) return TQ_ERR_INVALID;
+    if (w->cb.levels == 2 || w->cb.levels == 256) return TQ_ERR_UNSUPPORTED;
+    QmvParams p = make_params(w, x_rot, y, ydt, err);
+    p.mode = kModeMulti;
+    p.ids = ids;
+    p.k = 1;
+    return run(p, w->group, 1, P, as_stream(stream));
+}
+
+// ---------------------------------------------------------------- dequant_experts
+
+namespace {
+
+// One CTA per (selected expert, row): each thread decodes whole words.
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ codes,
+                                                      const uint16_t* __restrict__ scales, int64_t row_stride,
+                                                      int64_t esw, int64_t ess, int rows, int cols, int group,
+                                                      int experts, const float* __restrict__ centroids, int levels,
+                                                      const int32_t* __restrict__ ids, void* out, int odt,
+                                                      uint32_t* err) {
+    __shared__ float lut[256];
+    for (int i = threadIdx.x; i < levels; i += blockDim.x) lut[i] = centroids[i];
+    __syncthreads();
+    const int n = blockIdx.x;
+    const int64_t i_sel = blockIdx.y;
+    const int e = ids[i_sel];
+    const int64_t obase = (i_sel * rows + n) * (int64_t)cols;
+    const bool bad = e < 0 || e >= experts;
+    if (bad && threadIdx.x == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
+    const int cw = levels == 3 ? 20 : (levels == 8 ? 10 : 32 / (31 - __clz(levels)));
+    const int bits = 31 - __clz(levels);
+    const int nw = (cols + cw - 1) / cw;
+    const uint32_t* wr = codes + (bad ? 0 : (int64_t)e * esw + (int64_t)n * row_stride);
+    const uint16_t* sr = scales + (bad ? 0 : (int64_t)e * ess + (int64_t)n * (cols / group));
+    for (int j = threadIdx.x; j < nw; j += blockDim.x) {
+        const uint32_t w = bad ? 0u : wr[j];
+        if (levels == 3) {
+            const TritHalves th = trit_split(w);
+            uint32_t Fh = th.hi, Fl = th.lo;
+            uint32_t d[20];
+            for (int t = 0; t < 10; ++t) d[19 - t] = trit_next_int(Fh);
+            for (int t = 0; t < 10; ++t) d[9 - t] = trit_next_int(Fl);
+            for (int i = 0; i < 20; ++i) {
+                const int kk = j * 20 + i;
+                if (kk < cols)
+                    store_from_float(out, obase + kk, odt,
+                                     bad ? 0.f : half_bits_to_float(sr[kk / group]) * lut[d[i]]);
+            }
+        } else {
+            for (int i = 0; i < cw; ++i) {
+                const int kk = j * cw + i;
+                if (kk < cols) {
+                    const uint32_t c = (w >> (bits * i)) & ((1u << bits) - 1u);
+                    store_from_float(out, obase + kk, odt, bad ? 0.f : half_bits_to_float(sr[kk / group]) * lut[c]);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" tq_status tq_dequant_experts(const tq_qweight_t* w, const int32_t* ids, int32_t n_ids, void* out,
+                                        tq_dtype odt, uint32_t* err, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (n_ids < 0 || !(odt == TQ_F32 || odt == TQ_BF16 || odt == TQ_F16)) return TQ_ERR_INVALID;
+    if (n_ids == 0) return TQ_OK;
+    if (!ids || !out || n_ids > 65535) return TQ_ERR_INVALID;
+    dequant_kernel<<<dim3(w->rows, n_ids), 256, 0, as_stream(stream)>>>(
+        w->codes, w->scales, w->row_stride_words, w->experts > 1 ? w->expert_stride_words : 0,
+        w->experts > 1 ? w->expert_stride_scales : 0, w->rows, w->cols, w->group, w->experts, w->cb.centroids,
+        w->cb.levels, ids, out, odt, err);
+    return launch_status();
+}

@@ -1,0 +1,105 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared
+symbol, and its host-only entry points agree with the oracle.  No device work
+is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import tq_oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from rotated_codebook_quantized_gb300 import _build
+
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\*?\s+\*?(tq_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("tq_codebook", "tq_quantize", "tq_qmv", "tq_gather_qmv", "tq_multi_gather_qmv", "tq_gather_qmm",
+                 "tq_dequant_experts", "tq_kv_quantize", "tq_kv_attend", "tq_rotate", "tq_moe_route"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(clib):
+    for name in declared_functions():
+        assert hasattr(clib, name), name
+
+
+def test_binding_signatures_cover_the_header():
+    import rotated_codebook_quantized_gb300 as tq
+
+    assert sorted(tq._SIGS) == declared_functions()
+
+
+def test_host_codebook_matches_oracle():
+    import rotated_codebook_quantized_gb300 as tq
+
+    for L in (2, 3, 4, 8, 16, 256):
+        c, t = tq.codebook(L)
+        oc, ot = o.lloyd_max_gaussian(L)
+        # The 256-level fixed point is ill-conditioned (the Lloyd map contracts by
+        # about 1 - O(1/L^2)), so two converged solvers agree to ~1e-12, not 1e-15;
+        # the fp32 tables the kernels use must agree exactly.
+        tol = 1e-10 if L == 256 else 1e-12
+        np.testing.assert_allclose(c, oc, rtol=0, atol=tol)
+        np.testing.assert_allclose(t, ot, rtol=0, atol=tol)
+        np.testing.assert_array_equal(c.astype(np.float32), oc.astype(np.float32))
+        np.testing.assert_array_equal(t.astype(np.float32), ot.astype(np.float32))
+        np.testing.assert_array_equal(c, -c[::-1])
+
+
+def test_host_signs_match_oracle():
+    import rotated_codebook_quantized_gb300 as tq
+
+    for seed, dim in ((0, 17), (1234567, 5), (4001, 7168)):
+        np.testing.assert_array_equal(tq.rotation_signs(seed, dim), o.rotation_signs(seed, dim))
+
+
+def test_format_helpers_match_oracle():
+    import rotated_codebook_quantized_gb300 as tq
+
+    for L in (2, 3, 4, 8, 16, 256):
+        assert tq.codes_per_word(L) == o.codes_per_word(L)
+        for K in (1, 20, 21, 4096, 7168):
+            assert tq.row_words(L, K) == o.row_words(L, K)
+            assert tq.row_stride_words(L, K) == (o.row_words(L, K) + 3) // 4 * 4
+    assert tq.codes_per_word(5) == 0
+
+
+def test_host_validation_rejects_bad_arguments():
+    """Argument checks run on the host and return before any CUDA call."""
+    import rotated_codebook_quantized_gb300 as tq
+
+    lib = tq.load()
+    fake = ctypes.c_void_p(0x1000)
+    cb = tq.tq_codebook_t(8, fake.value, fake.value)
+    rot = tq.tq_rotation_t(512, 512, fake.value)
+    # group 48 is not a supported group size
+    assert lib.tq_quantize(fake, 0, 4, 512, 48, ctypes.byref(rot), ctypes.byref(cb), fake, fake, 52, None) == \
+        tq.TQ_ERR_INVALID
+    # rotation block that does not divide the dimension
+    bad_rot = tq.tq_rotation_t(512, 384, fake.value)
+    assert lib.tq_quantize(fake, 0, 4, 512, 64, ctypes.byref(bad_rot), ctypes.byref(cb), fake, fake, 52, None) == \
+        tq.TQ_ERR_INVALID
+    # row stride below the packed row length
+    assert lib.tq_quantize(fake, 0, 4, 512, 64, ctypes.byref(rot), ctypes.byref(cb), fake, fake, 12, None) == \
+        tq.TQ_ERR_INVALID
+    qw = tq.tq_qweight_t(fake.value, fake.value, 1, 64, 512, 64, 51, 0, 0, cb)  # stride not a multiple of 4
+    assert lib.tq_qmv(ctypes.byref(qw), fake, 1, fake, 0, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_moe_route(fake, 1, 2000, 8, fake, fake, fake, fake, fake, fake, 1 << 20, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_codebook(5, None, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_status_string(tq.TQ_ERR_TIMEOUT) == b"device wait timed out"
