@@ -171,9 +171,12 @@ __global__ void __launch_bounds__(256) kv_quantize_kernel(const void* __restrict
     }
 }
 
-int pick_e(int dim, int block) {
+// Elements per thread: smallest power of two E with whole warps (dim % 32E == 0),
+// at most 1024 threads, E <= block, and a group spread over at most one warp
+// (group / E <= 32) so the group's sum of squares is a warp-shuffle reduction.
+int pick_e(int dim, int block, int group) {
     for (int e = 1; e <= 16; e <<= 1)
-        if (e <= block && dim % (32 * e) == 0 && dim / e <= 1024) return e;
+        if (e <= block && dim % (32 * e) == 0 && dim / e <= 1024 && group <= 32 * e) return e;
     return 0;
 }
 
@@ -194,7 +197,7 @@ extern "C" tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int3
     if (!(cb->levels == 3 || cb->levels == 4 || cb->levels == 8 || cb->levels == 16)) return TQ_ERR_UNSUPPORTED;
     if (rows == 0) return TQ_OK;
     if (!W || !codes || !scales) return TQ_ERR_INVALID;
-    const int e = pick_e(cols, rot->block);
+    const int e = pick_e(cols, rot->block, group);
     if (e == 0 || cols > 16384) return TQ_ERR_UNSUPPORTED;
     const int threads = cols / e;
     const size_t smem = (size_t)cols * 4 + 256 * 4 + (size_t)cols;

@@ -111,7 +111,7 @@ def test_quantize_codes_and_scales(lib, levels, group, K, block, rows, wdt):
     near = compare_scales(f16_from_bits(e["scales"]), e["os16"], e["rms"])
     n = rows * K
     assert ties <= max(3, n // 20000), f"{ties} ties of {n}"
-    assert near <= max(3, n // 20000)
+    assert near <= max(3, (n // group) // 500)
 
 
 @pytest.mark.parametrize("levels,group,K,block,rows,wdt", QCASES)
@@ -125,8 +125,11 @@ def test_quantize_then_qmv(lib, levels, group, K, block, rows, wdt, T):
     y = lib.qmv(qw, xr).cpu().numpy()
     ref = o.qmv(o.dequantize(e["ocodes"], e["os16"], e["oc"], group), o.rotate(x, e["signs"], block))
     assert rel_l2(y, ref) < REL_L2
+    # bf16 output: the kernel's own fp32 result rounded once (nearest even), and
+    # within the bar of the oracle rounded to bf16 the same way.
     ybf = lib.qmv(qw, xr, out_dtype=torch.bfloat16).float().cpu().numpy()
-    assert rel_l2(ybf, ref) < REL_L2
+    np.testing.assert_array_equal(ybf, wl.to_bf16(y)[1])
+    assert rel_l2(ybf, wl.to_bf16(ref)[1]) < REL_L2
 
 
 def _random_bank(levels, experts, rows, K, group, seed):
@@ -322,8 +325,86 @@ def test_kv_quantize_and_attend(lib, T, klev, vlev, group):
         gw = u32(codes_d[:, :T]).reshape(Hkv * T, -1)
         ties = compare_codes(gw, ow, lev, D, u, t, what=name)
         near = compare_scales(f16_from_bits(scales_d[:, :T]).reshape(Hkv * T, -1), os16.reshape(Hkv * T, -1), rms)
-        assert ties <= max(3, T * Hkv * D // 20000) and near <= 3
+        # each counted case was checked above to sit at a tie / rounding midpoint;
+        # the counts only guard against a systematic shift
+        assert ties <= max(3, T * Hkv * D // 20000) and near <= max(3, T * Hkv * (D // group) // 500)
         outs[name] = o.dequantize(ocodes.reshape(Hkv * T, D), os16.reshape(Hkv * T, -1), c, group).reshape(Hkv, T, D)
     o_gpu = lib.kv_attend(cache, _bf16_dev(qb)).cpu().numpy()
     ref = o.kv_attend(q, outs["k"], outs["v"], signs)
     assert rel_l2(o_gpu, ref) < REL_L2
+
+
+def _qmm_case(lib, levels, group, E, rows, K, T, k, xt, seed):
+    """Encode an expert bank on both sides, route T tokens, run the gather-GEMM."""
+    bank = [wl.expert_weights(seed, e, 0, rows, K)[1] for e in range(E)]
+    signs = o.rotation_signs(wl.sign_seed(seed, 0), K)
+    blk = o.rotation_block(K)
+    rot = lib.Rotation(K, blk, signs=signs)
+    cb = lib.Codebook(levels)
+    codes, scales = lib.quantize(_dev(np.concatenate(bank)), group, rot, cb)
+    qw = lib.QWeight(codes, scales, E, rows, K, group, cb)
+    logits = wl.router_logits(seed, T, E, zipf=1.1)
+    _, x = wl.activations(seed, T, K)
+    ids, probs, perm, pos, off = lib.moe_route(_dev(logits), k)
+    dt = torch.float16 if xt == "f16" else torch.bfloat16
+    xr = lib.rotate(_dev(x), rot, out_dtype=dt)
+    y = lib.gather_qmm(qw, xr, perm, off, k).cpu().numpy()
+    oids, _ = o.route(logits, k)
+    operm, ooff = o.sort_pairs(oids, E)
+    oc, ot = o.lloyd_max_gaussian(levels)
+    R = o.rotation_matrix(signs, blk)
+    Wh = {}
+
+    def bankf(e):
+        if e not in Wh:
+            c, s16 = o.encode_rotated(bank[e].astype(np.float64) @ R.T, group, ot)
+            Wh[e] = o.dequantize(c, s16, oc, group)
+        return Wh[e]
+
+    ref = o.gather_qmm(bankf, o.rotate(x, signs, blk), operm, ooff, k)
+    return y, ref, ooff
+
+
+@pytest.mark.parametrize("levels,group,E,rows,K,T,k", [(8, 64, 12, 256, 1024, 300, 8), (16, 64, 6, 128, 512, 70, 2),
+                                                       (4, 32, 5, 128, 640, 40, 3), (8, 128, 3, 384, 1536, 9, 2)])
+def test_gather_qmm_tensor_core(lib, levels, group, E, rows, K, T, k):
+    y, ref, off = _qmm_case(lib, levels, group, E, rows, K, T, k, "f16", seed=4)
+    assert rel_l2(y, ref) < REL_L2
+    for e in range(E):  # every expert's block of sorted rows on its own
+        lo, hi = off[e], off[e + 1]
+        if hi > lo:
+            assert rel_l2(y[lo:hi], ref[lo:hi]) < REL_L2, e
+
+
+def test_gather_qmm_skew_spans_several_tiles(lib):
+    y, ref, off = _qmm_case(lib, 8, 64, 16, 128, 512, 700, 8, "f16", seed=41)
+    counts = np.diff(off)
+    assert counts.max() > 256
+    assert rel_l2(y, ref) < REL_L2
+
+
+def test_gather_qmm_bf16_operands(lib):
+    """bf16 operands: A and B rounded to 8-bit mantissas, error budget about 2 x 2^-9 / sqrt(3)."""
+    y, ref, _ = _qmm_case(lib, 8, 64, 6, 128, 512, 64, 4, "bf16", seed=43)
+    assert rel_l2(y, ref) < 4e-3
+
+
+def test_gather_qmm_per_pair_input(lib):
+    """Down-projection form: row i of x is sorted pair i's own input."""
+    E, rows, K, group, levels = 7, 256, 1536, 64, 8
+    bank = [wl.expert_weights(5, e, 1, rows, K)[1] for e in range(E)]
+    signs = o.rotation_signs(77, K)
+    rot = lib.Rotation(K, 512, signs=signs)
+    cb = lib.Codebook(levels)
+    codes, scales = lib.quantize(_dev(np.concatenate(bank)), group, rot, cb)
+    qw = lib.QWeight(codes, scales, E, rows, K, group, cb)
+    counts = np.array([0, 300, 5, 17, 0, 64, 1])
+    off = np.concatenate(([0], np.cumsum(counts))).astype(np.int32)
+    P = int(off[-1])
+    h = wl.rng(6, P).normal(size=(P, K)).astype(np.float16)
+    y = lib.gather_qmm(qw, _dev(h), _dev(np.zeros(P, np.int32)), _dev(off), 1, per_pair_input=True).cpu().numpy()
+    oc, ot = o.lloyd_max_gaussian(levels)
+    R = o.rotation_matrix(signs, 512)
+    Wh = [o.dequantize(*o.encode_rotated(bank[e].astype(np.float64) @ R.T, group, ot), oc, group) for e in range(E)]
+    ref = o.gather_qmm(lambda e: Wh[e], h.astype(np.float64), np.arange(P), off, 1, per_pair_input=True)
+    assert rel_l2(y, ref) < REL_L2
