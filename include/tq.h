@@ -275,6 +275,33 @@ tq_status tq_kv_attend(const void* q, tq_dtype qdt, int32_t Hq, int32_t Hkv, int
                        const uint16_t* vscales, float* o, void* ws, size_t ws_bytes, void* stream);
 size_t tq_kv_attend_workspace_bytes(int32_t Hq, int32_t D, int64_t ctx);
 
+/* tq_kv_attend without a caller-supplied workspace.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory where they run attention: for example a
+ * serving process whose device memory is all handed out up front by its own
+ * pool, or a plug-in inside a host framework that owns every device buffer
+ * and gives the plug-in no allocator.  cudaMalloc and cudaFree can also
+ * synchronise the device, which a latency-bound decode loop may not accept.
+ * Arguments and results are those of tq_kv_attend minus ws / ws_bytes.  The
+ * split-context partial results live instead in a fixed array of
+ * tq_kv_attend_noalloc_max_scratch_bytes() bytes (4 MiB) inside the library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits.  No memory is allocated by the call (no cudaMalloc, cudaFree or
+ * allocating library routine).  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current) and
+ * caches it; make that first call before any stream capture.  Sizes whose
+ * scratch, tq_kv_attend_workspace_bytes(Hq, D, ctx), exceeds the maximum
+ * return TQ_ERR_INVALID without launching.  All calls on a device share the
+ * array, which keeps the previous call's contents (every slot a call reads is
+ * first written by that call); calls whose kernels overlap on the GPU, e.g.
+ * on two streams, race on it and must be serialised by the caller. */
+tq_status tq_kv_attend_noalloc(const void* q, tq_dtype qdt, int32_t Hq, int32_t Hkv, int32_t D, int64_t ctx,
+                               int64_t capacity, const tq_rotation_t* rot, const tq_codebook_t* kcb,
+                               const tq_codebook_t* vcb, int32_t group, const uint32_t* kcodes,
+                               const uint16_t* kscales, const uint32_t* vcodes, const uint16_t* vscales, float* o,
+                               void* stream);
+size_t tq_kv_attend_noalloc_max_scratch_bytes(void);
+
 /* Waits for `stream`, reads the device error word and clears it.
  * Returns TQ_OK if it was 0, TQ_ERR_TIMEOUT if TQ_DEVERR_TIMEOUT is set, else
  * TQ_ERR_DEVICE; *bits (host, may be NULL) receives the word. */

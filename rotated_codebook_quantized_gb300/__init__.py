@@ -69,6 +69,9 @@ _SIGS = {
     "tq_kv_attend": (_i32, [_c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t), _P(tq_codebook_t),
                             _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _sz, _c_p]),
     "tq_kv_attend_workspace_bytes": (_sz, [_i32, _i32, _i64]),
+    "tq_kv_attend_noalloc": (_i32, [_c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t), _P(tq_codebook_t),
+                                    _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "tq_kv_attend_noalloc_max_scratch_bytes": (_sz, []),
     "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
     "tq_selftest_trit_decode": (_i32, [_u32, _u32, _c_p, _c_p]),
 }
@@ -382,6 +385,21 @@ def kv_attend(cache: KVCache, q, ctx: int | None = None, ws=None):
                                ctypes.byref(kb), ctypes.byref(vb), cache.group, _ptr(cache.kcodes),
                                _ptr(cache.kscales), _ptr(cache.vcodes), _ptr(cache.vscales), _ptr(o), _ptr(ws),
                                ws.numel(), _stream()), "tq_kv_attend")
+    return o
+
+
+def kv_attend_noalloc(cache: KVCache, q, ctx: int | None = None):
+    """kv_attend with the library's fixed device scratch instead of a workspace (see include/tq.h)."""
+    torch = _torch()
+    _contig(q, "q")
+    Hq = q.shape[0]
+    ctx = cache.length if ctx is None else ctx
+    o = torch.empty((Hq, cache.dim), dtype=torch.float32, device=q.device)
+    r, kb, vb = cache.rot.c(), cache.kcb.c(), cache.vcb.c()
+    _check(load().tq_kv_attend_noalloc(_ptr(q), _dt(q), Hq, cache.heads, cache.dim, ctx, cache.capacity,
+                                       ctypes.byref(r), ctypes.byref(kb), ctypes.byref(vb), cache.group,
+                                       _ptr(cache.kcodes), _ptr(cache.kscales), _ptr(cache.vcodes),
+                                       _ptr(cache.vscales), _ptr(o), _stream()), "tq_kv_attend_noalloc")
     return o
 
 

@@ -14,6 +14,8 @@
 // kernel merges the chunks and de-rotates.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 using namespace tq;
@@ -249,4 +251,53 @@ extern "C" tq_status tq_kv_attend(const void* q, tq_dtype qdt, int32_t Hq, int32
     if (s != TQ_OK) return s;
     kv_merge_kernel<<<Hq, 32, 0, st>>>(part, Hq, (int)nsplit, rot->signs, o);
     return launch_status();
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+
+namespace {
+
+// Scratch of the allocation-free entry point: a fixed array in the library's
+// device image.  Every GPU that loads the library holds it until the process
+// exits; all calls on a device share it.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) float g_kv_attend_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The host-side
+// name of a __device__ array is only a stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+tq_status noalloc_scratch(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kv_attend_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<float*>(g_scratch_addr[dev]);
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tq_kv_attend_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" tq_status tq_kv_attend_noalloc(const void* q, tq_dtype qdt, int32_t Hq, int32_t Hkv, int32_t D, int64_t ctx,
+                                          int64_t capacity, const tq_rotation_t* rot, const tq_codebook_t* kcb,
+                                          const tq_codebook_t* vcb, int32_t group, const uint32_t* kcodes,
+                                          const uint16_t* kscales, const uint32_t* vcodes, const uint16_t* vscales,
+                                          float* o, void* stream) {
+    const size_t need = tq_kv_attend_workspace_bytes(Hq, D, ctx);
+    if (need == 0 || need > kNoAllocScratchBytes) return TQ_ERR_INVALID;
+    float* ws = nullptr;
+    const tq_status s = noalloc_scratch(&ws);
+    if (s != TQ_OK) return s;
+    return tq_kv_attend(q, qdt, Hq, Hkv, D, ctx, capacity, rot, kcb, vcb, group, kcodes, kscales, vcodes, vscales, o,
+                        ws, kNoAllocScratchBytes, stream);
 }
