@@ -155,8 +155,8 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- device bank
 
-def make_bank(torch, tq, dev):
-    """Timing bank of 384 ternary experts with random valid words and fp16 scales (device-generated)."""
+def make_bank(torch, tq, dev, E=E):
+    """Timing bank of E ternary experts with random valid words and fp16 scales (device-generated)."""
     cb = tq.Codebook(3, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + SEED)
@@ -181,6 +181,71 @@ def make_bank(torch, tq, dev):
     return qgu, qdn
 
 
+# ---------------------------------------------------------------- MoE prefill gather-GEMM
+
+P_E, P_T, P_K, P_H, P_I, P_G = 128, 4096, 8, 4096, 1536, 64
+P_SEED = 4
+
+
+def random_bit_bank(torch, tq, dev, gen, experts, rows, cols, levels, group):
+    """Random valid bit-packed words (unused slots and padding zero) and fp16 scales."""
+    cw = tq.codes_per_word(levels)
+    bits = {4: 2, 8: 3, 16: 4}[levels]
+    nw = tq.row_words(levels, cols)
+    stride = tq.row_stride_words(levels, cols)
+    codes = torch.zeros((experts, rows, stride), dtype=torch.int32, device=dev)
+    sc = torch.empty((experts, rows, cols // group), dtype=torch.float16, device=dev)
+    for e in range(experts):
+        w = torch.randint(0, 1 << (bits * cw), (rows, nw), generator=gen, device=dev, dtype=torch.int64)
+        used = cols - (nw - 1) * cw
+        w[:, -1] &= (1 << (bits * used)) - 1
+        codes[e, :, :nw] = (w - (w >= 2 ** 31).long() * 2 ** 32).to(torch.int32)
+        sc[e].copy_(torch.exp(torch.randn(sc[e].shape, generator=gen, device=dev) * 0.5 - 3.5))
+    cb = tq.Codebook(levels, device=dev)
+    return tq.QWeight(codes, sc.view(torch.int16), experts, rows, cols, group, cb, row_stride=stride)
+
+
+def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
+    """gate||up and down gather_qmm over 4096 tokens routed top-8 of 128 experts (Zipf-skewed)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + P_SEED)
+    qgu = random_bit_bank(torch, tq, dev, gen, P_E, 2 * P_I, P_H, 8, P_G)
+    qdn = random_bit_bank(torch, tq, dev, gen, P_E, P_H, P_I, 8, P_G)
+    logits = torch.from_numpy(wl.router_logits(P_SEED, P_T, P_E, zipf=1.1)).to(dev)
+    ids, probs, perm, pos, off = tq.moe_route(logits, P_K)
+    x = torch.randn((P_T, P_H), generator=gen, device=dev).half()
+    h = torch.randn((P_T * P_K, P_I), generator=gen, device=dev).half()
+    P = P_T * P_K
+    for _ in range(2):
+        tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)
+        tq.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)
+        ev[i][1].record()
+        tq.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True, out_dtype=torch.bfloat16)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    t_gu = sorted(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))[iters // 2]
+    t_dn = sorted(ev[i][1].elapsed_time(ev[i][2]) for i in range(iters))[iters // 2]
+    f_gu = 2.0 * P * (2 * P_I) * P_H
+    f_dn = 2.0 * P * P_H * P_I
+    tf = (f_gu + f_dn) / ((t_gu + t_dn) * 1e-3) / 1e12
+    counts = (off[1:] - off[:-1]).cpu()
+    return {"metric": "MoE prefill gather_qmm TFLOP/s", "value": tf, "unit": "TFLOP/s",
+            "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "peak": peaks["bf16_tflops"],
+            "peak_source": peaks["source"] + " (bf16 burst; fp16 operands have the same dense rate)",
+            "flops_per_step": f_gu + f_dn, "ms_gate_up": t_gu, "ms_down": t_dn,
+            "tflops_gate_up": f_gu / (t_gu * 1e-3) / 1e12, "tflops_down": f_dn / (t_dn * 1e-3) / 1e12,
+            "config": {"tokens": P_T, "experts": P_E, "top_k": P_K, "hidden": P_H, "intermediate": P_I,
+                       "bits": 3, "group": P_G, "operands": "fp16", "output": "bf16",
+                       "router": "N(0,1) + Zipf(1.1) bias", "max_pairs_per_expert": int(counts.max()),
+                       "min_pairs_per_expert": int(counts.min())}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -188,6 +253,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--experts", type=int, default=E, help="decode bank size (smaller only for profiling captures)")
+    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill gather-GEMM measurement")
     ap.add_argument("--_oracle-sample", dest="oracle_sample", type=float, default=None)
     args = ap.parse_args()
 
@@ -206,7 +273,7 @@ def main():
               "experts": E, "top_k": TOPK, "hidden": HIDDEN, "intermediate": INTER, "group": GROUP,
               "tokens_per_step": 1, "bytes_per_step": step_bytes,
               "cache": "L2 flushed (256 MiB write) before every timed step; 5.5 GB expert bank, fresh routing per step"}
-    metric = "MoE gather_qmv decode packed-weight GB/s"
+    metric = "MoE gather_qmv decode packed-weight GB/s (% HBM peak); gather_qmm TFLOP/s"
 
     if args.impl == "reference":
         if rank != 0:
@@ -228,7 +295,7 @@ def main():
                           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
 
-    cpu = cpu_baseline_subprocess(args.cpu_seconds) if rank == 0 else None
+    cpu = cpu_baseline_subprocess(args.cpu_seconds) if rank == 0 and args.cpu_seconds > 0 else None
 
     import torch
 
@@ -244,15 +311,16 @@ def main():
     tq.load()
     peaks = measured_peaks()
 
-    qgu, qdn = make_bank(torch, tq, dev)
+    nexp = args.experts
+    qgu, qdn = make_bank(torch, tq, dev, nexp)
     rotH = tq.Rotation(HIDDEN, 1024, seed=wl.sign_seed(SEED, 0), device=dev)
     rotI = tq.Rotation(INTER, 2048, seed=wl.sign_seed(SEED, 1), device=dev)
     nsteps = args.warmup + args.steps
-    logits_all = torch.from_numpy(wl.router_logits(SEED + 17 * rank, nsteps, E)).to(dev)
+    logits_all = torch.from_numpy(wl.router_logits(SEED + 17 * rank, nsteps, nexp)).to(dev)
     x_all = torch.from_numpy(wl.activations(SEED + 17 * rank, nsteps, HIDDEN)[0].view("int16")).to(dev).view(
         torch.bfloat16)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    logits_buf = torch.empty((1, E), dtype=torch.float32, device=dev)
+    logits_buf = torch.empty((1, nexp), dtype=torch.float32, device=dev)
     x_buf = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device=dev)
 
     def step():
@@ -310,7 +378,7 @@ def main():
     clocks = clk.summary()
 
     # dominant kernel alone: gate||up gather_qmv, one launch per replay, L2 flushed between
-    ids_fixed = torch.tensor([[3, 77, 120, 191, 250, 301, 333, 383]], dtype=torch.int32, device=dev)
+    ids_fixed = torch.tensor([[(3 + 47 * j) % nexp for j in range(TOPK)]], dtype=torch.int32, device=dev)
     xr_fixed = tq.rotate(x_all[0:1], rotH)
     gs = torch.cuda.Stream(device=dev)
     gs.wait_stream(torch.cuda.current_stream())
@@ -330,7 +398,7 @@ def main():
     k_ms = sum(kt) / len(kt)
     k_bytes = TOPK * gu_b
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    roofline = {"kernel": "qmv_kernel<3,16,1> (gate||up gather_qmv, 8 experts)", "bound": "hbm",
+    roofline = {"kernel": "qmv_trit_kernel<16,4> (gate||up gather_qmv, 8 ternary experts)", "bound": "hbm",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
                 "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_ms * 1e3}
@@ -341,7 +409,7 @@ def main():
             roofline["traffic"] = d
 
     # end to end through the Python API: pinned host inputs in, result out, every step
-    h_logits = torch.from_numpy(wl.router_logits(SEED + 17 * rank + 5, nsteps, E)).pin_memory()
+    h_logits = torch.from_numpy(wl.router_logits(SEED + 17 * rank + 5, nsteps, nexp)).pin_memory()
     h_x = torch.from_numpy(wl.activations(SEED + 17 * rank + 5, nsteps, HIDDEN)[0].view("int16")).pin_memory()
     h_out = torch.empty((nsteps, HIDDEN), dtype=torch.float32).pin_memory()
     d_x = torch.empty((1, HIDDEN), dtype=torch.int16, device=dev)
@@ -363,8 +431,10 @@ def main():
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     e2e = {"value": world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": E * 4 + HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
+           "h2d_bytes_per_step": nexp * 4 + HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
            "ms_per_step": e2e_ms / args.steps}
+
+    prefill = None if args.skip_prefill else measure_prefill(torch, tq, wl, dev, flush, peaks)
 
     if rank == 0:
         line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -372,6 +442,7 @@ def main():
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
                 "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+                "gather_qmm_tflops": prefill["value"] if prefill else None, "prefill": prefill,
                 "wall_s_timed_loop": wall}
         print(json.dumps(line))
     if world > 1:

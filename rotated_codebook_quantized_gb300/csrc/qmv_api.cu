@@ -62,6 +62,7 @@ QmvParams make_params(const tq_qweight_t* w, const float* x, void* y, tq_dtype y
 }
 
 tq_status run(const QmvParams& p, int group, int nv, int n_items, cudaStream_t st) {
+    if (p.levels == 3 && nv == 1) return qmv_trit_run(p, group, n_items, st);
 #define TQ_QMV_G(L)                                                     \
     switch (group) {                                                    \
         case 16: return qmv_run_l##L##_g16(p, nv, n_items, st);         \

@@ -1,0 +1,287 @@
+// Ternary inline-decode matvec (one input vector per item): the kernel behind
+// tq_qmv / tq_gather_qmv / tq_multi_gather_qmv for three-level books.
+//
+// "How it works", "The ternary tier (1.58 bits)": 20 trits per 32-bit word in
+// base 3; "Running a quantized layer": decode inline, no per-weight integer
+// division.
+//
+// Decode.  A word w = sum_j d_j 3^j is split into two ten-digit halves
+// (w / 3^10 is a multiply by a constant).  Each half h becomes the 32-bit
+// fixed-point fraction F = h*72736 + 8860 (in [h, h+1) 2^32/3^10 for every h),
+// and mul.hi(F, 81) yields the next four digits as one number v in [0, 81)
+// (mul.hi(F, 9) the last two).  v indexes a per-lane copy of an 81-entry table
+// in shared memory whose entry packs the four digits into four bytes; two
+// dp2a instructions multiply them by the input, which is held as 16-bit
+// integers (per group: x = xs_g * xq, |xq| <= 32767).  The three-level book is
+// affine (c0 + d*delta), so per group
+//     sum_k c[d_k] x_k = delta * xs_g * (sum_k d_k xq_k) + c0 * sum_k x_k,
+// an exact integer dot product plus two precomputed per-group terms.
+//
+// Work layout.  A warp takes RPW rows of one item and walks their columns in
+// steps of UPW consecutive units (RPW * UPW = 32 lanes): lane (r, c) decodes
+// unit s*UPW + c of row r.  A load instruction thus covers RPW contiguous
+// segments of UPW units (coalesced), and the UPW units in flight read their
+// quantized input from shared-memory blocks that start on distinct 4-bank
+// groups, shared by the RPW lanes of each unit (broadcast).  CTAs are
+// persistent: each takes a contiguous range of (item, row block) tasks,
+// prepares the quantized input once per distinct input vector, and its warps
+// share the tasks round-robin.
+#include <numeric>
+
+#include "qmv_impl.cuh"
+
+namespace tq {
+namespace {
+
+template <int G>
+struct TritFmt {
+    static constexpr int kUT = 20 / Gcd<20, G>::v * G;  // trits per unit: lcm(20, G)
+    static constexpr int kUW = kUT / 20;                // words per unit
+    static constexpr int kGPU = kUT / G;                // groups per unit
+    static constexpr int kXW = 12;                      // shared words of 16-bit x pairs per code word (10 used)
+    static constexpr int kAB = kUW * kXW;               // offset of the (a_g, b_g) floats in a unit block
+    static constexpr int kRaw = kAB + 2 * kGPU;
+    // unit block stride: whole 16-byte chunks, = 4 (mod 8) words so that 8
+    // consecutive units start on distinct 4-bank groups
+    static constexpr int kUS = ((kRaw + 3) / 4 * 4) % 8 == 4 ? (kRaw + 3) / 4 * 4 : (kRaw + 3) / 4 * 4 + 4;
+};
+
+TQ_DEVFN uint32_t dp2a_lo(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+TQ_DEVFN uint32_t dp2a_hi(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+struct TritParams {
+    QmvParams q;
+    int units;      // units per row
+    int nsteps;     // steps of UPW units per row
+    int tasks_per_item;
+    int n_items;
+    int total_tasks;
+};
+
+template <int G, int RPW>
+__global__ void __launch_bounds__(256, 2) qmv_trit_kernel(const TritParams tp) {
+    using F = TritFmt<G>;
+    constexpr int UPW = 32 / RPW;
+    constexpr int UW = F::kUW, GPU = F::kGPU, US = F::kUS;
+    const QmvParams& p = tp.q;
+    extern __shared__ __align__(16) uint32_t sm[];
+    uint32_t* lut = sm;            // [81][32]: per-lane copies, entry v of lane l at v*32 + l
+    uint32_t* xb = lut + 81 * 32;  // [nsteps*UPW units][US]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    for (int i = tid; i < 81 * 32; i += blockDim.x) {
+        const int v = i >> 5;
+        lut[i] = (uint32_t)(v / 27) | ((uint32_t)((v / 9) % 3) << 8) | ((uint32_t)((v / 3) % 3) << 16) |
+                 ((uint32_t)(v % 3) << 24);
+    }
+    // centroid c[d] = c0 + d * delta (three-level affine book)
+    const float c0 = __ldg(p.centroids), delta = __ldg(p.centroids + 1) - c0;
+    if (tid == 0 && p.err && fabsf((__ldg(p.centroids + 2) - __ldg(p.centroids + 1)) - delta) > 1e-6f * fabsf(delta))
+        atomicOr(p.err, TQ_DEVERR_BAD_BOOK);
+
+    const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
+    const int t_end = (int)((int64_t)(blockIdx.x + 1) * tp.total_tasks / gridDim.x);
+    const int r = lane / UPW, c = lane % UPW;
+    const uint32_t* lut_lane = lut + lane;
+    const int ngroups = p.ngroups;
+    const int nunits_pad = tp.nsteps * UPW;
+    int cur_vec = -1;
+
+    for (int t0 = t_begin; t0 < t_end;) {
+        const int item = t0 / tp.tasks_per_item;
+        const int t1 = min(t_end, (item + 1) * tp.tasks_per_item);
+        int e, vec;
+        if (p.mode == kModeDense) {
+            e = 0;
+            vec = item;
+        } else {
+            e = __ldg(p.ids + item);
+            vec = p.mode == kModeGather ? item / p.k : item;
+        }
+        const int64_t out0 = (int64_t)item * p.rows;
+        if (vec != cur_vec) {
+            // Quantize this vector per group: xs = max|x| / 32767, xq = rint(x / xs),
+            // a_g = delta * xs, b_g = c0 * sum(x); zero beyond the last column.
+            __syncthreads();
+            const float* xv = p.x + (int64_t)vec * p.cols;
+            for (int g = tid; g < nunits_pad * GPU; g += blockDim.x) {
+                const int u = g / GPU, gl = g - u * GPU;  // unit, group within the unit
+                float mx = 0.f, sum = 0.f;
+                if (g < ngroups) {
+#pragma unroll 8
+                    for (int k = 0; k < G; ++k) {
+                        const float v = xv[g * G + k];
+                        mx = fmaxf(mx, fabsf(v));
+                        sum += v;
+                    }
+                }
+                uint32_t* blk = xb + u * US;
+                reinterpret_cast<float*>(blk + F::kAB)[2 * gl] = delta * (mx / 32767.0f);
+                reinterpret_cast<float*>(blk + F::kAB)[2 * gl + 1] = c0 * sum;
+                const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+                // pair pp of word w holds the 16-bit inputs of unit trits (20w + 19 - 2pp, 20w + 18 - 2pp)
+#pragma unroll 4
+                for (int k = 0; k < G; k += 2) {
+                    const int tl = gl * G + k;  // even unit-local trit
+                    const int w = tl / 20, pp = (18 - (tl - 20 * w)) / 2;
+                    const int tg = g * G + k;   // global trit
+                    const float xlo = g < ngroups ? xv[tg] : 0.f;
+                    const float xhi = g < ngroups ? xv[tg + 1] : 0.f;
+                    const int qlo = __float2int_rn(xlo * inv), qhi = __float2int_rn(xhi * inv);
+                    blk[w * F::kXW + pp] = ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16);
+                }
+            }
+            __syncthreads();
+            cur_vec = vec;
+        }
+        const bool bad = e < 0 || e >= p.experts;
+        if (bad && tid == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+
+        for (int t = t0 + warp; t < t1; t += nwarps) {
+            const int row = (t - item * tp.tasks_per_item) * RPW + r;
+            const int rowc = row < p.rows ? row : p.rows - 1;
+            float tot = 0.f;
+            if (!bad) {
+                const uint32_t* wrow = p.codes + (int64_t)e * p.expert_stride_w + (int64_t)rowc * p.row_stride;
+                const uint16_t* srow = p.scales + (int64_t)e * p.expert_stride_s + (int64_t)rowc * ngroups;
+                // prefetch depth in steps: about 64 bytes of codes in flight per lane
+                constexpr int PF = UW >= 16 ? 1 : (UW == 8 ? 2 : 4);
+                uint32_t wb[PF][UW];
+                float sb[PF][GPU];
+                auto load = [&](int s, uint32_t (&W)[UW], float (&S)[GPU]) {
+                    const int u = s * UPW + c;
+#pragma unroll
+                    for (int m = 0; m < UW; m += 4) {
+                        const int64_t wi = (int64_t)u * UW + m;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (wi < p.row_stride) v = ldg_u4(wrow + wi);
+                        W[m] = v.x;
+                        W[m + 1] = v.y;
+                        W[m + 2] = v.z;
+                        W[m + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int g = 0; g < GPU; ++g) {
+                        const int gg = u * GPU + g;
+                        S[g] = gg < ngroups ? half_bits_to_float(__ldg(srow + gg)) : 0.f;
+                    }
+                };
+#pragma unroll
+                for (int i = 0; i < PF - 1; ++i)
+                    if (i < tp.nsteps) load(i, wb[i], sb[i]);
+                for (int s0 = 0; s0 < tp.nsteps; s0 += PF) {
+#pragma unroll
+                    for (int uu = 0; uu < PF; ++uu) {
+                        const int s = s0 + uu;
+                        if (s < tp.nsteps) {
+                            if (s + PF - 1 < tp.nsteps) load(s + PF - 1, wb[(uu + PF - 1) % PF], sb[(uu + PF - 1) % PF]);
+                            uint32_t acc[GPU];
+#pragma unroll
+                            for (int g = 0; g < GPU; ++g) acc[g] = 0u;
+                            const uint32_t* blk = xb + (s * UPW + c) * US;
+#pragma unroll
+                            for (int w = 0; w < UW; ++w) {
+                                const uint4 xa = *reinterpret_cast<const uint4*>(blk + w * F::kXW);
+                                const uint4 xc = *reinterpret_cast<const uint4*>(blk + w * F::kXW + 4);
+                                const uint2 xd = *reinterpret_cast<const uint2*>(blk + w * F::kXW + 8);
+                                const uint32_t xp[10] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w, xd.x, xd.y};
+                                const uint32_t word = wb[uu][w];
+                                const uint32_t hh = word / 59049u;
+                                const uint32_t ll = word - hh * 59049u;
+#pragma unroll
+                                for (int half = 0; half < 2; ++half) {
+                                    uint32_t Fx = (half == 0 ? hh : ll) * 72736u + 8860u;
+                                    const int pb = half * 5;  // first pair of this half
+                                    // digits 4 at a time (v in [0, 81)), then the last 2 (v in [0, 9))
+                                    const uint32_t v1 = __umulhi(Fx, 81u);
+                                    Fx *= 81u;
+                                    const uint32_t v2 = __umulhi(Fx, 81u);
+                                    Fx *= 81u;
+                                    const uint32_t v3 = __umulhi(Fx, 9u);
+                                    const uint32_t e1 = lut_lane[v1 << 5], e2 = lut_lane[v2 << 5], e3 = lut_lane[v3 << 5];
+                                    // group of pair pp of word w: unit-local trit (20w + 18 - 2pp) / G
+#define TQ_GRP(pp) ((20 * w + 18 - 2 * (pp)) / G)
+                                    acc[TQ_GRP(pb + 0)] = dp2a_lo(xp[pb + 0], e1, acc[TQ_GRP(pb + 0)]);
+                                    acc[TQ_GRP(pb + 1)] = dp2a_hi(xp[pb + 1], e1, acc[TQ_GRP(pb + 1)]);
+                                    acc[TQ_GRP(pb + 2)] = dp2a_lo(xp[pb + 2], e2, acc[TQ_GRP(pb + 2)]);
+                                    acc[TQ_GRP(pb + 3)] = dp2a_hi(xp[pb + 3], e2, acc[TQ_GRP(pb + 3)]);
+                                    acc[TQ_GRP(pb + 4)] = dp2a_hi(xp[pb + 4], e3, acc[TQ_GRP(pb + 4)]);
+#undef TQ_GRP
+                                }
+                            }
+                            const float* abu = reinterpret_cast<const float*>(blk + F::kAB);
+#pragma unroll
+                            for (int g = 0; g < GPU; ++g)
+                                tot = fmaf(sb[uu][g], fmaf(abu[2 * g], (float)(int)acc[g], abu[2 * g + 1]), tot);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 1; m < UPW; m <<= 1) tot += __shfl_xor_sync(kFull, tot, m);
+            if (c == 0 && row < p.rows) store_from_float(p.y, out0 + row, p.ydt, tot);
+        }
+        t0 = t1;
+    }
+}
+
+template <int G, int RPW>
+tq_status launch_trit(const QmvParams& qp, int n_items, cudaStream_t st) {
+    using F = TritFmt<G>;
+    constexpr int UPW = 32 / RPW;
+    TritParams tp{};
+    tp.q = qp;
+    tp.units = (qp.cols + F::kUT - 1) / F::kUT;
+    tp.nsteps = (tp.units + UPW - 1) / UPW;
+    tp.tasks_per_item = (qp.rows + RPW - 1) / RPW;
+    tp.n_items = n_items;
+    const int64_t total = (int64_t)n_items * tp.tasks_per_item;
+    if (total > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    tp.total_tasks = (int)total;
+    const size_t smem = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * UPW * F::kUS);
+    if (smem > 200 * 1024) return TQ_ERR_UNSUPPORTED;
+    const void* kfn = (const void*)qmv_trit_kernel<G, RPW>;
+    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_trit_kernel<G, RPW>, 256, smem) != cudaSuccess ||
+        per_sm <= 0)
+        per_sm = 1;
+    int64_t grid = (int64_t)sms * per_sm;
+    const int64_t max_grid = (total + 7) / 8;  // at least one task per warp
+    if (grid > max_grid) grid = max_grid;
+    if (grid < 1) grid = 1;
+    qmv_trit_kernel<G, RPW><<<(unsigned)grid, 256, smem, st>>>(tp);
+    return launch_status();
+}
+
+}  // namespace
+
+// Rows per warp step: 4 rows x 8 units when a row holds many units, else 8 rows
+// x 4 units (keeps the last, partial step of short rows cheap).
+tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t st) {
+    const int ut = 20 / std::gcd(20, group) * group;
+    const bool wide = (p.cols + ut - 1) / ut >= 48;
+    switch (group) {
+        case 16: return wide ? launch_trit<16, 4>(p, n_items, st) : launch_trit<16, 8>(p, n_items, st);
+        case 32: return wide ? launch_trit<32, 4>(p, n_items, st) : launch_trit<32, 8>(p, n_items, st);
+        case 64: return wide ? launch_trit<64, 4>(p, n_items, st) : launch_trit<64, 8>(p, n_items, st);
+        case 128: return wide ? launch_trit<128, 4>(p, n_items, st) : launch_trit<128, 8>(p, n_items, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace tq

@@ -132,6 +132,13 @@ def test_quantize_then_qmv(lib, levels, group, K, block, rows, wdt, T):
     assert rel_l2(ybf, wl.to_bf16(ref)[1]) < REL_L2
 
 
+def _decode_tol(levels):
+    """Decode-only tolerance.  Bit-packed books: fp32 arithmetic only (1e-5).  The
+    ternary kernel holds the input as 16-bit integers per group (error <= max|x|/65534
+    per element, at most sqrt(G) times the group RMS: about 3.5e-5 relative), so 1e-4."""
+    return 1e-4 if levels == 3 else 1e-5
+
+
 def _random_bank(levels, experts, rows, K, group, seed):
     """Random valid packed words and fp16 scales (timing-style bank), uint32 / float16 numpy."""
     g = wl.rng(seed, 99)
@@ -179,7 +186,7 @@ def test_qmv_decode_exact(lib, levels, group, K, rows):
     for T in (1, 2, 4):
         y = lib.qmv(qw, _dev(x[:T].astype(np.float32))).cpu().numpy()
         ref = o.qmv(Wh(0), x[:T].astype(np.float32))
-        assert rel_l2(y, ref) < 1e-5, T
+        assert rel_l2(y, ref) < _decode_tol(levels), T
 
 
 def test_gather_qmv_and_bad_ids(lib):
@@ -191,14 +198,14 @@ def test_gather_qmv_and_bad_ids(lib):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = lib.gather_qmv(qw, _dev(x), _dev(ids), err=err).cpu().numpy()
     ref = o.gather_qmv(Wh, ids, x)
-    assert rel_l2(y, ref) < 1e-5
+    assert rel_l2(y, ref) < _decode_tol(3)
     assert lib.check_error(err) == 0
     bad = ids.copy()
     bad[1, 2] = 12
     y = lib.gather_qmv(qw, _dev(x), _dev(bad), err=err).cpu().numpy()
     assert lib.check_error(err) == lib.TQ_DEVERR_BAD_ID
     assert np.all(y[1, 2] == 0)
-    assert rel_l2(y[0], ref[0]) < 1e-5
+    assert rel_l2(y[0], ref[0]) < _decode_tol(3)
 
 
 def test_multi_gather_qmv(lib):
@@ -207,7 +214,7 @@ def test_multi_gather_qmv(lib):
     ids = np.array([8, 0, 8, 4, 4, 1, 2], dtype=np.int32)
     x = wl.rng(6).normal(size=(len(ids), K)).astype(np.float32)
     y = lib.multi_gather_qmv(qw, _dev(x), _dev(ids)).cpu().numpy()
-    assert rel_l2(y, o.multi_gather_qmv(Wh, ids, x)) < 1e-5
+    assert rel_l2(y, o.multi_gather_qmv(Wh, ids, x)) < _decode_tol(3)
 
 
 def test_dequant_experts(lib):
