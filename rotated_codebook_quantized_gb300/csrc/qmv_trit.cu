@@ -268,11 +268,274 @@ tq_status launch_trit(const QmvParams& qp, int n_items, cudaStream_t st) {
     return launch_status();
 }
 
+// ---------------------------------------------------------------- pipelined variant
+//
+// Same decode, but codes and scales are staged in a per-warp ring of NS
+// shared-memory stages with cp.async (16 bytes per lane, one commit group per
+// stage and lane), so NS-1 stages are in flight while the warp decodes the
+// oldest one and no registers hold data in flight.  A stage holds 8
+// consecutive units of each of the warp's 4 rows: their code words
+// (8 * UW * 4 bytes per row) followed by their 40 fp16 scales (80 bytes per
+// row).  Each cp.async instruction covers 4 contiguous 128-byte row segments.
+// (1-D bulk copies were measured at about one request per 38 cycles per SM,
+// too slow for 128-byte pieces.)
+
+TQ_DEVFN uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+TQ_DEVFN void cp16(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+TQ_DEVFN void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+TQ_DEVFN void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kPipeNS = 5;  // stages per warp ring
+constexpr int kPipeRPW = 4, kPipeUPW = 8;
+
+template <int G>
+struct PipeFmt {
+    using F = TritFmt<G>;
+    static constexpr int kCodeBytes = kPipeUPW * F::kUW * 4;       // per row and stage
+    static constexpr int kScaleBytes = kPipeUPW * F::kGPU * 2;     // per row and stage (80)
+    static constexpr int kStage = kPipeRPW * (kCodeBytes + kScaleBytes);
+};
+
+template <int G>
+__global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams tp) {
+    using F = TritFmt<G>;
+    using B = PipeFmt<G>;
+    constexpr int RPW = kPipeRPW, UPW = kPipeUPW, NS = kPipeNS;
+    constexpr int UW = F::kUW, GPU = F::kGPU, US = F::kUS;
+    const QmvParams& p = tp.q;
+    extern __shared__ __align__(16) uint32_t sm[];
+    uint32_t* lut = sm;                                           // [81][32]
+    uint32_t* xb = lut + 81 * 32;                                 // [nsteps*8 units][US]
+    const int nunits_pad = tp.nsteps * UPW;
+    uint8_t* ring0 = reinterpret_cast<uint8_t*>(xb + nunits_pad * US);  // [8 warps][NS][stage]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int nwarps = 8;
+    for (int i = tid; i < 81 * 32; i += blockDim.x) {
+        const int v = i >> 5;
+        lut[i] = (uint32_t)(v / 27) | ((uint32_t)((v / 9) % 3) << 8) | ((uint32_t)((v / 3) % 3) << 16) |
+                 ((uint32_t)(v % 3) << 24);
+    }
+    const float c0 = __ldg(p.centroids), delta = __ldg(p.centroids + 1) - c0;
+    if (tid == 0 && p.err && fabsf((__ldg(p.centroids + 2) - __ldg(p.centroids + 1)) - delta) > 1e-6f * fabsf(delta))
+        atomicOr(p.err, TQ_DEVERR_BAD_BOOK);
+
+    const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
+    const int t_end = (int)((int64_t)(blockIdx.x + 1) * tp.total_tasks / gridDim.x);
+    const int r = lane / UPW, c = lane % UPW;
+    const uint32_t* lut_lane = lut + lane;
+    const int ngroups = p.ngroups;
+    const int nst = tp.nsteps;  // stages (of 8 units) per task
+    uint8_t* ring = ring0 + warp * NS * B::kStage;
+    int cur_vec = -1;
+
+    for (int t0 = t_begin; t0 < t_end;) {
+        const int item = t0 / tp.tasks_per_item;
+        const int t1 = min(t_end, (item + 1) * tp.tasks_per_item);
+        int e, vec;
+        if (p.mode == kModeDense) {
+            e = 0;
+            vec = item;
+        } else {
+            e = __ldg(p.ids + item);
+            vec = p.mode == kModeGather ? item / p.k : item;
+        }
+        const int64_t out0 = (int64_t)item * p.rows;
+        if (vec != cur_vec) {
+            __syncthreads();
+            const float* xv = p.x + (int64_t)vec * p.cols;
+            for (int g = tid; g < nunits_pad * GPU; g += blockDim.x) {
+                const int u = g / GPU, gl = g - u * GPU;
+                float mx = 0.f, sum = 0.f;
+                if (g < ngroups) {
+#pragma unroll 8
+                    for (int k = 0; k < G; ++k) {
+                        const float v = xv[g * G + k];
+                        mx = fmaxf(mx, fabsf(v));
+                        sum += v;
+                    }
+                }
+                uint32_t* blk = xb + u * US;
+                reinterpret_cast<float*>(blk + F::kAB)[2 * gl] = delta * (mx / 32767.0f);
+                reinterpret_cast<float*>(blk + F::kAB)[2 * gl + 1] = c0 * sum;
+                const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+#pragma unroll 4
+                for (int k = 0; k < G; k += 2) {
+                    const int tl = gl * G + k;
+                    const int w = tl / 20, pp = (18 - (tl - 20 * w)) / 2;
+                    const int tg = g * G + k;
+                    const float xlo = g < ngroups ? xv[tg] : 0.f;
+                    const float xhi = g < ngroups ? xv[tg + 1] : 0.f;
+                    const int qlo = __float2int_rn(xlo * inv), qhi = __float2int_rn(xhi * inv);
+                    blk[w * F::kXW + pp] = ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16);
+                }
+            }
+            __syncthreads();
+            cur_vec = vec;
+        }
+        const bool bad = e < 0 || e >= p.experts;
+        if (bad && tid == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+
+        // this warp's tasks in the item: t0 + warp + 8k
+        const int n_my = (t1 - t0 - warp + nwarps - 1) / nwarps;
+        const int L = n_my > 0 ? n_my * nst : 0;
+        const uint32_t* cbase = p.codes + (int64_t)(bad ? 0 : e) * p.expert_stride_w;
+        const uint16_t* sbase = p.scales + (int64_t)(bad ? 0 : e) * p.expert_stride_s;
+        // Stage j of this item goes to slot j % NS; every lane commits one group per stage.
+        auto issue = [&](int j) {
+            const int t = t0 + warp + (j / nst) * nwarps;
+            const int st = j % nst;
+            uint8_t* dst = ring + (j % NS) * B::kStage;
+            const int row = min((t - item * tp.tasks_per_item) * RPW + r, p.rows - 1);
+            const int64_t w0 = (int64_t)(st * UPW + c) * UW;  // this lane's unit
+            const uint32_t* csrc = cbase + (int64_t)row * p.row_stride;
+#pragma unroll
+            for (int m = 0; m < UW; m += 4) {
+                const int64_t wi = w0 + m;
+                cp16(dst + r * B::kCodeBytes + (c * UW + m) * 4, csrc + (wi < p.row_stride ? wi : 0),
+                     wi < p.row_stride ? 16u : 0u);
+            }
+            if (c < B::kScaleBytes / 16) {  // 5 lanes per row copy its 80 bytes of scales
+                const int64_t g0 = (int64_t)st * UPW * GPU + c * 8;
+                const int64_t left = (int64_t)ngroups - g0;
+                const uint32_t nb = left >= 8 ? 16u : (left > 0 ? (uint32_t)left * 2u : 0u);
+                cp16(dst + RPW * B::kCodeBytes + r * B::kScaleBytes + c * 16,
+                     sbase + (int64_t)row * ngroups + (left > 0 ? g0 : 0), nb);
+            }
+            cp_commit();
+        };
+        for (int j = 0; j < NS - 1; ++j) {
+            if (j < L) issue(j); else cp_commit();
+        }
+        float tot = 0.f;
+        for (int j = 0; j < L; ++j) {
+            cp_wait<NS - 2>();
+            __syncwarp();
+            const int slot = j % NS;
+            const int st = j % nst;
+            const int u = st * UPW + c;
+            const uint8_t* stg = ring + slot * B::kStage;
+            if (u < tp.units && !bad) {
+                uint32_t acc[GPU];
+#pragma unroll
+                for (int g = 0; g < GPU; ++g) acc[g] = 0u;
+                const uint32_t* blk = xb + u * US;
+                const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(stg + r * B::kCodeBytes + c * UW * 4);
+#pragma unroll
+                for (int w4 = 0; w4 < UW; w4 += 4) {
+                    const uint4 wq = *reinterpret_cast<const uint4*>(wsrc + w4);
+                    const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const int w = w4 + wi;
+                        const uint4 xa = *reinterpret_cast<const uint4*>(blk + w * F::kXW);
+                        const uint4 xc = *reinterpret_cast<const uint4*>(blk + w * F::kXW + 4);
+                        const uint2 xd = *reinterpret_cast<const uint2*>(blk + w * F::kXW + 8);
+                        const uint32_t xp[10] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w, xd.x, xd.y};
+                        const uint32_t word = wv[wi];
+                        const uint32_t hh = word / 59049u;
+                        const uint32_t ll = word - hh * 59049u;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t Fx = (half == 0 ? hh : ll) * 72736u + 8860u;
+                            const int pb = half * 5;
+                            const uint32_t v1 = __umulhi(Fx, 81u);
+                            Fx *= 81u;
+                            const uint32_t v2 = __umulhi(Fx, 81u);
+                            Fx *= 81u;
+                            const uint32_t v3 = __umulhi(Fx, 9u);
+                            const uint32_t e1 = lut_lane[v1 << 5], e2 = lut_lane[v2 << 5], e3 = lut_lane[v3 << 5];
+#define TQ_GRP(pp) ((20 * w + 18 - 2 * (pp)) / G)
+                            acc[TQ_GRP(pb + 0)] = dp2a_lo(xp[pb + 0], e1, acc[TQ_GRP(pb + 0)]);
+                            acc[TQ_GRP(pb + 1)] = dp2a_hi(xp[pb + 1], e1, acc[TQ_GRP(pb + 1)]);
+                            acc[TQ_GRP(pb + 2)] = dp2a_lo(xp[pb + 2], e2, acc[TQ_GRP(pb + 2)]);
+                            acc[TQ_GRP(pb + 3)] = dp2a_hi(xp[pb + 3], e2, acc[TQ_GRP(pb + 3)]);
+                            acc[TQ_GRP(pb + 4)] = dp2a_hi(xp[pb + 4], e3, acc[TQ_GRP(pb + 4)]);
+#undef TQ_GRP
+                        }
+                    }
+                }
+                const uint16_t* ssrc =
+                    reinterpret_cast<const uint16_t*>(stg + RPW * B::kCodeBytes + r * B::kScaleBytes) + c * GPU;
+                const float* abu = reinterpret_cast<const float*>(blk + F::kAB);
+#pragma unroll
+                for (int g = 0; g < GPU; ++g) {
+                    const float sv = (u * GPU + g < ngroups) ? half_bits_to_float(ssrc[g]) : 0.f;
+                    tot = fmaf(sv, fmaf(abu[2 * g], (float)(int)acc[g], abu[2 * g + 1]), tot);
+                }
+            }
+            if (st == nst - 1) {  // task done: reduce the row over its 8 lanes
+                float v = tot;
+#pragma unroll
+                for (int m = 1; m < UPW; m <<= 1) v += __shfl_xor_sync(kFull, v, m);
+                const int t = t0 + warp + (j / nst) * nwarps;
+                const int row = (t - item * tp.tasks_per_item) * RPW + r;
+                if (c == 0 && row < p.rows) store_from_float(p.y, out0 + row, p.ydt, v);
+                tot = 0.f;
+            }
+            __syncwarp();
+            if (j + NS - 1 < L) issue(j + NS - 1); else cp_commit();
+        }
+        cp_wait<0>();
+        __syncwarp();
+        t0 = t1;
+    }
+}
+
+template <int G>
+tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
+    using F = TritFmt<G>;
+    using B = PipeFmt<G>;
+    TritParams tp{};
+    tp.q = qp;
+    tp.units = (qp.cols + F::kUT - 1) / F::kUT;
+    tp.nsteps = (tp.units + kPipeUPW - 1) / kPipeUPW;
+    tp.tasks_per_item = (qp.rows + kPipeRPW - 1) / kPipeRPW;
+    tp.n_items = n_items;
+    const int64_t total = (int64_t)n_items * tp.tasks_per_item;
+    if (total > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    tp.total_tasks = (int)total;
+    const size_t smem = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * kPipeUPW * F::kUS) +
+                        (size_t)8 * kPipeNS * B::kStage;
+    if (smem > 200 * 1024) return TQ_ERR_UNSUPPORTED;
+    const void* kfn = (const void*)qmv_trit_pipe_kernel<G>;
+    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_trit_pipe_kernel<G>, 256, smem) != cudaSuccess ||
+        per_sm <= 0)
+        per_sm = 1;
+    int64_t grid = (int64_t)sms * per_sm;
+    const int64_t max_grid = (total + 7) / 8;
+    if (grid > max_grid) grid = max_grid;
+    if (grid < 1) grid = 1;
+    qmv_trit_pipe_kernel<G><<<(unsigned)grid, 256, smem, st>>>(tp);
+    return launch_status();
+}
+
 }  // namespace
 
 // Rows per warp step: 4 rows x 8 units when a row holds many units, else 8 rows
 // x 4 units (keeps the last, partial step of short rows cheap).
 tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t st) {
+    // Staged pipeline when every copy is 16-byte aligned: 16-byte code rows
+    // (always), scale rows and expert scale strides in whole 16-byte chunks.
+    const bool pipe_ok = (group == 16 || group == 32) && ((int64_t)p.ngroups * 2) % 16 == 0 &&
+                         (p.expert_stride_s * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.codes) & 15) == 0;
+    if (pipe_ok) return group == 16 ? launch_trit_pipe<16>(p, n_items, st) : launch_trit_pipe<32>(p, n_items, st);
     const int ut = 20 / std::gcd(20, group) * group;
     const bool wide = (p.cols + ut - 1) / ut >= 48;
     switch (group) {
