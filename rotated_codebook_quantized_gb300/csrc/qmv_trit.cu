@@ -309,15 +309,16 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
     using B = PipeFmt<G>;
     constexpr int RPW = kPipeRPW, UPW = kPipeUPW, NS = kPipeNS;
     constexpr int UW = F::kUW, GPU = F::kGPU, US = F::kUS;
+    constexpr int nwarps = 8;
     const QmvParams& p = tp.q;
     extern __shared__ __align__(16) uint32_t sm[];
     uint32_t* lut = sm;                                           // [81][32]
     uint32_t* xb = lut + 81 * 32;                                 // [nsteps*8 units][US]
     const int nunits_pad = tp.nsteps * UPW;
     uint8_t* ring0 = reinterpret_cast<uint8_t*>(xb + nunits_pad * US);  // [8 warps][NS][stage]
+    float* rowsum = reinterpret_cast<float*>(ring0 + nwarps * NS * B::kStage);  // [max tasks per CTA][RPW]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int nwarps = 8;
     for (int i = tid; i < 81 * 32; i += blockDim.x) {
         const int v = i >> 5;
         lut[i] = (uint32_t)(v / 27) | ((uint32_t)((v / 9) % 3) << 8) | ((uint32_t)((v / 3) % 3) << 16) |
@@ -333,13 +334,11 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
     const uint32_t* lut_lane = lut + lane;
     const int ngroups = p.ngroups;
     const int nst = tp.nsteps;  // stages (of 8 units) per task
+    const int tpi = tp.tasks_per_item;
     uint8_t* ring = ring0 + warp * NS * B::kStage;
     int cur_vec = -1;
 
-    for (int t0 = t_begin; t0 < t_end;) {
-        const int item = t0 / tp.tasks_per_item;
-        const int t1 = min(t_end, (item + 1) * tp.tasks_per_item);
-        int e, vec;
+    auto item_info = [&](int item, int& e, int& vec) {
         if (p.mode == kModeDense) {
             e = 0;
             vec = item;
@@ -347,82 +346,134 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
             e = __ldg(p.ids + item);
             vec = p.mode == kModeGather ? item / p.k : item;
         }
-        const int64_t out0 = (int64_t)item * p.rows;
+    };
+
+    // Segments: maximal runs of this CTA's tasks whose items share one input vector.
+    for (int s0 = t_begin; s0 < t_end;) {
+        int e0, vec;
+        item_info(s0 / tpi, e0, vec);
+        int s1 = min(t_end, (s0 / tpi + 1) * tpi);
+        while (s1 < t_end) {  // extend over following items with the same vector
+            int e1, v1;
+            item_info(s1 / tpi, e1, v1);
+            if (v1 != vec) break;
+            s1 = min(t_end, (s1 / tpi + 1) * tpi);
+        }
+        __syncthreads();  // previous segment's row sums written out, x no longer read
+
+        // This warp's share of the segment's (task, stage) units: a contiguous range.
+        const int nunits_seg = (s1 - s0) * nst;
+        const int f_begin = (int)((int64_t)warp * nunits_seg / nwarps);
+        const int f_end = (int)((int64_t)(warp + 1) * nunits_seg / nwarps);
+        const int L = f_end - f_begin;
+
+        // producer position (task, stage) and its row pointers
+        int pt = s0 + f_begin / nst, ps = f_begin % nst, pslot = 0;
+        const uint32_t* pcode = nullptr;
+        const uint16_t* pscale = nullptr;
+        auto set_prod_task = [&]() {
+            int e, v;
+            item_info(pt / tpi, e, v);
+            if (e < 0 || e >= p.experts) e = 0;  // rows of a bad id are written as zero below
+            const int row = min((pt % tpi) * RPW + r, p.rows - 1);
+            pcode = p.codes + (int64_t)e * p.expert_stride_w + (int64_t)row * p.row_stride;
+            pscale = p.scales + (int64_t)e * p.expert_stride_s + (int64_t)row * ngroups;
+        };
+        if (L > 0) set_prod_task();
+        auto issue = [&]() {
+            uint8_t* dst = ring + pslot * B::kStage;
+            const int64_t w0 = (int64_t)(ps * UPW + c) * UW;  // this lane's unit
+#pragma unroll
+            for (int m = 0; m < UW; m += 4) {
+                const int64_t wi = w0 + m;
+                const bool in = wi < p.row_stride;
+                cp16(dst + r * B::kCodeBytes + (c * UW + m) * 4, pcode + (in ? wi : 0), in ? 16u : 0u);
+            }
+            if (c < B::kScaleBytes / 16) {  // 5 lanes per row copy its 80 bytes of scales
+                const int64_t g0 = (int64_t)ps * UPW * GPU + c * 8;
+                const bool in = g0 < ngroups;  // scale rows are whole 16-byte chunks
+                cp16(dst + RPW * B::kCodeBytes + r * B::kScaleBytes + c * 16, pscale + (in ? g0 : 0), in ? 16u : 0u);
+            }
+            cp_commit();
+            pslot = pslot + 1 == NS ? 0 : pslot + 1;
+            if (++ps == nst) {
+                ps = 0;
+                ++pt;
+                if (pt < s1) set_prod_task();
+            }
+        };
+        // weights start streaming before the input is prepared
+        for (int j = 0; j < NS - 1; ++j) {
+            if (j < L) issue(); else cp_commit();
+        }
+
+        for (int i = tid; i < (s1 - s0) * RPW; i += blockDim.x) rowsum[i] = 0.f;
         if (vec != cur_vec) {
-            __syncthreads();
+            // Quantize this vector per group: xs = max|x| / 32767, xq = rint(x / xs),
+            // a_g = delta * xs, b_g = c0 * sum(x); zero beyond the last column.
+            // One thread per group, the group's values read once into registers.
             const float* xv = p.x + (int64_t)vec * p.cols;
+            const bool x16 = (reinterpret_cast<uintptr_t>(xv) & 15) == 0;
             for (int g = tid; g < nunits_pad * GPU; g += blockDim.x) {
                 const int u = g / GPU, gl = g - u * GPU;
-                float mx = 0.f, sum = 0.f;
+                float xr[G];
                 if (g < ngroups) {
-#pragma unroll 8
-                    for (int k = 0; k < G; ++k) {
-                        const float v = xv[g * G + k];
-                        mx = fmaxf(mx, fabsf(v));
-                        sum += v;
+                    if (x16) {
+#pragma unroll
+                        for (int k = 0; k < G; k += 4) {
+                            const float4 v4 = __ldg(reinterpret_cast<const float4*>(xv + g * G + k));
+                            xr[k] = v4.x;
+                            xr[k + 1] = v4.y;
+                            xr[k + 2] = v4.z;
+                            xr[k + 3] = v4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < G; ++k) xr[k] = __ldg(xv + g * G + k);
                     }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < G; ++k) xr[k] = 0.f;
+                }
+                float mx = 0.f, sum = 0.f;
+#pragma unroll
+                for (int k = 0; k < G; ++k) {
+                    mx = fmaxf(mx, fabsf(xr[k]));
+                    sum += xr[k];
                 }
                 uint32_t* blk = xb + u * US;
                 reinterpret_cast<float*>(blk + F::kAB)[2 * gl] = delta * (mx / 32767.0f);
                 reinterpret_cast<float*>(blk + F::kAB)[2 * gl + 1] = c0 * sum;
                 const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
-#pragma unroll 4
+#pragma unroll
                 for (int k = 0; k < G; k += 2) {
+                    // pair of unit-local trits (tl, tl + 1), tl even, lives at pair pp of word w
                     const int tl = gl * G + k;
                     const int w = tl / 20, pp = (18 - (tl - 20 * w)) / 2;
-                    const int tg = g * G + k;
-                    const float xlo = g < ngroups ? xv[tg] : 0.f;
-                    const float xhi = g < ngroups ? xv[tg + 1] : 0.f;
-                    const int qlo = __float2int_rn(xlo * inv), qhi = __float2int_rn(xhi * inv);
+                    const int qlo = __float2int_rn(xr[k] * inv), qhi = __float2int_rn(xr[k + 1] * inv);
                     blk[w * F::kXW + pp] = ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16);
                 }
             }
-            __syncthreads();
             cur_vec = vec;
         }
-        const bool bad = e < 0 || e >= p.experts;
-        if (bad && tid == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+        __syncthreads();
 
-        // this warp's tasks in the item: t0 + warp + 8k
-        const int n_my = (t1 - t0 - warp + nwarps - 1) / nwarps;
-        const int L = n_my > 0 ? n_my * nst : 0;
-        const uint32_t* cbase = p.codes + (int64_t)(bad ? 0 : e) * p.expert_stride_w;
-        const uint16_t* sbase = p.scales + (int64_t)(bad ? 0 : e) * p.expert_stride_s;
-        // Stage j of this item goes to slot j % NS; every lane commits one group per stage.
-        auto issue = [&](int j) {
-            const int t = t0 + warp + (j / nst) * nwarps;
-            const int st = j % nst;
-            uint8_t* dst = ring + (j % NS) * B::kStage;
-            const int row = min((t - item * tp.tasks_per_item) * RPW + r, p.rows - 1);
-            const int64_t w0 = (int64_t)(st * UPW + c) * UW;  // this lane's unit
-            const uint32_t* csrc = cbase + (int64_t)row * p.row_stride;
-#pragma unroll
-            for (int m = 0; m < UW; m += 4) {
-                const int64_t wi = w0 + m;
-                cp16(dst + r * B::kCodeBytes + (c * UW + m) * 4, csrc + (wi < p.row_stride ? wi : 0),
-                     wi < p.row_stride ? 16u : 0u);
-            }
-            if (c < B::kScaleBytes / 16) {  // 5 lanes per row copy its 80 bytes of scales
-                const int64_t g0 = (int64_t)st * UPW * GPU + c * 8;
-                const int64_t left = (int64_t)ngroups - g0;
-                const uint32_t nb = left >= 8 ? 16u : (left > 0 ? (uint32_t)left * 2u : 0u);
-                cp16(dst + RPW * B::kCodeBytes + r * B::kScaleBytes + c * 16,
-                     sbase + (int64_t)row * ngroups + (left > 0 ? g0 : 0), nb);
-            }
-            cp_commit();
-        };
-        for (int j = 0; j < NS - 1; ++j) {
-            if (j < L) issue(j); else cp_commit();
+        // consumer position
+        int ct = s0 + f_begin / nst, cs = f_begin % nst, cslot = 0;
+        bool cbad;
+        {
+            int e, v;
+            item_info(ct / tpi, e, v);
+            cbad = e < 0 || e >= p.experts;
+            if (cbad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
         }
         float tot = 0.f;
         for (int j = 0; j < L; ++j) {
             cp_wait<NS - 2>();
             __syncwarp();
-            const int slot = j % NS;
-            const int st = j % nst;
-            const int u = st * UPW + c;
-            const uint8_t* stg = ring + slot * B::kStage;
-            if (u < tp.units && !bad) {
+            const int u = cs * UPW + c;
+            const uint8_t* stg = ring + cslot * B::kStage;
+            if (u < tp.units && !cbad) {
                 uint32_t acc[GPU];
 #pragma unroll
                 for (int g = 0; g < GPU; ++g) acc[g] = 0u;
@@ -471,21 +522,34 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
                     tot = fmaf(sv, fmaf(abu[2 * g], (float)(int)acc[g], abu[2 * g + 1]), tot);
                 }
             }
-            if (st == nst - 1) {  // task done: reduce the row over its 8 lanes
+            cslot = cslot + 1 == NS ? 0 : cslot + 1;
+            if (++cs == nst || j == L - 1) {  // task finished or this warp's share ends: add the row sums
                 float v = tot;
 #pragma unroll
                 for (int m = 1; m < UPW; m <<= 1) v += __shfl_xor_sync(kFull, v, m);
-                const int t = t0 + warp + (j / nst) * nwarps;
-                const int row = (t - item * tp.tasks_per_item) * RPW + r;
-                if (c == 0 && row < p.rows) store_from_float(p.y, out0 + row, p.ydt, v);
+                if (c == 0) atomicAdd(rowsum + (ct - s0) * RPW + r, v);
                 tot = 0.f;
+                if (cs == nst) {
+                    cs = 0;
+                    ++ct;
+                    if (ct < s1) {
+                        int e, vv;
+                        item_info(ct / tpi, e, vv);
+                        cbad = e < 0 || e >= p.experts;
+                        if (cbad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+                    }
+                }
             }
             __syncwarp();
-            if (j + NS - 1 < L) issue(j + NS - 1); else cp_commit();
+            if (j + NS - 1 < L) issue(); else cp_commit();
         }
         cp_wait<0>();
-        __syncwarp();
-        t0 = t1;
+        __syncthreads();  // all row sums of the segment complete
+        for (int i = tid; i < (s1 - s0) * RPW; i += blockDim.x) {
+            const int t = s0 + i / RPW, row = (t % tpi) * RPW + i % RPW;
+            if (row < p.rows) store_from_float(p.y, (int64_t)(t / tpi) * p.rows + row, p.ydt, rowsum[i]);
+        }
+        s0 = s1;
     }
 }
 
@@ -502,25 +566,34 @@ tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
     const int64_t total = (int64_t)n_items * tp.tasks_per_item;
     if (total > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
     tp.total_tasks = (int)total;
-    const size_t smem = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * kPipeUPW * F::kUS) +
-                        (size_t)8 * kPipeNS * B::kStage;
-    if (smem > 200 * 1024) return TQ_ERR_UNSUPPORTED;
-    const void* kfn = (const void*)qmv_trit_pipe_kernel<G>;
-    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    int max_grid_tasks = 0;  // tasks of the largest CTA range, for the row-sum buffer
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
+    const size_t smem_fixed = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * kPipeUPW * F::kUS) +
+                              (size_t)8 * kPipeNS * B::kStage;
+    const void* kfn = (const void*)qmv_trit_pipe_kernel<G>;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_trit_pipe_kernel<G>, 256, smem) != cudaSuccess ||
-        per_sm <= 0)
+    // occupancy with a row-sum buffer of up to 256 tasks (the limit must be raised first)
+    if (smem_fixed + 4096 > 200 * 1024) return TQ_ERR_UNSUPPORTED;
+    if (ensure_smem(kfn, smem_fixed + 4096) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_trit_pipe_kernel<G>, 256,
+                                                      smem_fixed + 4096) != cudaSuccess || per_sm <= 0)
         per_sm = 1;
+    // one wave of resident CTAs, but at most 128 tasks per CTA (bounds the row-sum buffer)
     int64_t grid = (int64_t)sms * per_sm;
     const int64_t max_grid = (total + 7) / 8;
     if (grid > max_grid) grid = max_grid;
+    if (grid < (total + 127) / 128) grid = (total + 127) / 128;
     if (grid < 1) grid = 1;
+    if (grid > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    max_grid_tasks = (int)((total + grid - 1) / grid) + 1;
+    const size_t smem = smem_fixed + (size_t)max_grid_tasks * kPipeRPW * 4;
+    if (smem > 200 * 1024) return TQ_ERR_UNSUPPORTED;
+    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
     qmv_trit_pipe_kernel<G><<<(unsigned)grid, 256, smem, st>>>(tp);
     return launch_status();
 }
