@@ -20,6 +20,8 @@
 // (expert, 128-row tile, 256-pair tile) in expert-major order so that CTAs
 // running together share the expert's codes in L2.  Every wait on an mbarrier
 // is bounded; on expiry the CTA sets TQ_DEVERR_TIMEOUT, drains and frees TMEM.
+#include <type_traits>
+
 #include "common.cuh"
 
 using namespace tq;
@@ -492,6 +494,454 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
     }
 }
 
+// ---------------------------------------------------------------- staged variant
+//
+// Same contraction and tile walk as gather_qmm_kernel, with the data movement
+// reorganised so that neither the copies nor the decode starve the tensor core:
+//   warp 0      issues the MMAs (one thread);
+//   warps 1-2   gather the pairs' input rows: each thread keeps the source row
+//               indices of its 32 rows in registers for the whole tile and
+//               issues one 16-byte cp.async per row and stage, 8 lanes per
+//               128-byte row segment (3-stage ring of 256 x 64 operand tiles);
+//   warp 3      stages the m-tile's scale block and its packed codes, 32 words
+//               (128 bytes) per row and chunk, in a 2-slot ring; word w of row r
+//               is stored at word w ^ (r & 31) of the row so that the decoders'
+//               reads (one word of 32 consecutive rows) are free of bank conflicts;
+//   warps 4-19  decode in two groups of 8 warps taking alternate stages: pairs
+//               of codes index a per-lane copy of a table of packed operand
+//               pairs and one half2 multiply applies s_group / s_rowmax; then
+//               all 16 drain the accumulator (epilogue).
+constexpr int kStagesA = 4, kStagesB = 3, kChunkSlots = 2;
+constexpr int kChunkBytes = kBM * 128;   // 32 code words of each of the 128 rows
+constexpr int kScaleBlock = kBM * 128;   // up to 64 fp16 scales of each row
+constexpr int kDec2 = 16;                // decoder warps
+constexpr int kFirstDec2 = 4;
+constexpr int kThreads2 = 32 * (kFirstDec2 + kDec2);
+constexpr int kDecThreads2 = 32 * kDec2;
+
+template <int LEVELS>
+struct Q2Fmt {
+    using F = BitFmt<LEVELS>;
+    static constexpr int kSPC = F::kCW / 2;                    // stages (64 codes) per 32-word chunk
+    static constexpr int kLutCopies = LEVELS == 16 ? 1 : 32;  // per-lane copies when small enough
+};
+
+template <int XT>
+TQ_DEVFN uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    if constexpr (XT == 0) {
+        __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    } else {
+        __nv_bfloat162 r =
+            __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+}
+
+TQ_DEVFN uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+TQ_DEVFN uint32_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+TQ_DEVFN void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+TQ_DEVFN void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+template <int LEVELS, int G, int XT>
+__global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmParams p) {
+    using F = BitFmt<LEVELS>;
+    using Q = Q2Fmt<LEVELS>;
+    constexpr int SPC = Q::kSPC, NL = LEVELS * LEVELS, COPIES = Q::kLutCopies;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;                                      // [4][128 x 64]
+    uint8_t* sB = sA + kStagesA * kABytes;                   // [3][256 x 64]
+    uint8_t* sC = sB + kStagesB * kBBytes;                   // [2][128 rows x 128 B] code chunks
+    uint8_t* sS = sC + kChunkSlots * kChunkBytes;            // [128 rows x 128 B] scale block
+    uint32_t* lut = reinterpret_cast<uint32_t*>(sS + kScaleBlock);       // [NL][COPIES] operand pairs
+    float* rowscale = reinterpret_cast<float*>(lut + NL * COPIES);       // [128]
+    float* rowmax_part = rowscale + kBM;                                 // [4][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(rowmax_part + 4 * kBM);
+    uint64_t* fullA = bars;
+    uint64_t* emptyA = fullA + kStagesA;
+    uint64_t* fullB = emptyA + kStagesA;
+    uint64_t* emptyB = fullB + kStagesB;
+    uint64_t* cfull = emptyB + kStagesB;
+    uint64_t* cempty = cfull + kChunkSlots;
+    uint64_t* sfull = cempty + kChunkSlots;
+    uint64_t* sempty = sfull + 1;
+    uint64_t* tile_full = sempty + 1;
+    uint64_t* tile_empty = tile_full + 1;
+    uint64_t* drain = tile_empty + 1;
+    uint64_t* decbar = drain + 1;
+    int* ctl = reinterpret_cast<int*>(decbar + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl);
+    volatile int* abort_flag = ctl + 1;
+    int* total_items = ctl + 2;
+    int* cum = ctl + 8;  // [experts + 1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.experts;
+    const int mtiles = p.rows / kBM;
+    const int nk = p.cols / kBK;
+    const int ngroups = p.cols / G;
+    const int nchunks = (nk + SPC - 1) / SPC;
+
+    for (int i = tid; i <= E; i += kThreads2) cum[i] = p.offsets[i];
+    for (int i = tid; i < NL * COPIES; i += kThreads2) {
+        const int idx = i / COPIES;
+        lut[i] = pack2<XT>(p.centroids[idx & (LEVELS - 1)], p.centroids[idx / LEVELS]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        bool ok = cum[0] == 0 && cum[E] == p.P;
+        int prev = 0, acc = 0;
+        for (int e = 0; e <= E; ++e) {
+            const int off = cum[e];
+            if (e > 0) {
+                const int n = off - prev;
+                ok = ok && n >= 0;
+                const int nt = n > 0 ? (n + kNT - 1) / kNT : 0;
+                cum[e - 1] = acc;
+                acc += nt * mtiles;
+            }
+            prev = off;
+        }
+        cum[E] = acc;
+        *total_items = ok ? acc : -1;
+        *abort_flag = 0;
+        for (int s = 0; s < kStagesA; ++s) {
+            mbar_init(fullA + s, 32 * kDec2 / 2);
+            mbar_init(emptyA + s, 1);
+        }
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(fullB + s, 64);
+            mbar_init(emptyB + s, 1);
+        }
+        for (int s = 0; s < kChunkSlots; ++s) {
+            mbar_init(cfull + s, 32);
+            mbar_init(cempty + s, kDecThreads2);
+        }
+        mbar_init(sfull, 32);
+        mbar_init(sempty, kDecThreads2);
+        mbar_init(tile_full, 1);
+        mbar_init(tile_empty, kDecThreads2);
+        mbar_init(drain, 1);
+        mbar_init(decbar, kDecThreads2);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int total = *total_items;
+    if (total < 0) {
+        if (tid == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+        return;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kNT)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto item_coords = [&](int item, int& e, int& mt, int& nt, int& i0, int& nvalid) {
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        e = lo;
+        const int off0 = p.offsets[e], n = p.offsets[e + 1] - off0;
+        const int ntiles = (n + kNT - 1) / kNT;
+        const int local = item - cum[e];
+        mt = local / ntiles;
+        nt = local - mt * ntiles;
+        i0 = off0 + nt * kNT;
+        nvalid = min(kNT, n - nt * kNT);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            uint32_t it = 0, tile_it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
+                int e, mt, nt, i0, nvalid;
+                item_coords(item, e, mt, nt, i0, nvalid);
+                const uint32_t idesc = f16_idesc(XT, (nvalid + 15) & ~15);
+                if (!mbar_wait(tile_empty, (tile_it & 1) ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const int sa = it % kStagesA, sb = it % kStagesB;
+                    if (!mbar_wait(fullA + sa, (it / kStagesA) & 1, abort_flag) ||
+                        !mbar_wait(fullB + sb, (it / kStagesB) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(a0 + sa * kABytes), bd = sw128_desc(b0 + sb * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
+                    tc_commit(emptyA + sa);
+                    tc_commit(emptyB + sb);
+                }
+                if (!ok) break;
+                tc_commit(tile_full);
+            }
+            tc_commit(drain);
+            if (!mbar_wait_drain(drain, 0)) *abort_flag = 1;
+        }
+        __syncwarp();
+    } else if (warp < 3) {
+        // ------------------------------------------------ B producers: rows rb + 8 i of every stage
+        const int t = tid - 32;            // 0..63
+        const int q = t & 7, rb = t >> 3;  // 16-byte piece; first row (rows rb + 8 i share r & 7 == rb)
+        const uint8_t* xq = reinterpret_cast<const uint8_t*>(p.x) + q * 16;
+        const uint32_t pitch = (uint32_t)p.cols * 2u;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            int e, mt, nt, i0, nvalid;
+            item_coords(item, e, mt, nt, i0, nvalid);
+            const int ninst = (nvalid + 15) & ~15;
+            const int cnt = (ninst - rb + 7) >> 3;  // my rows below ninst (ninst >= 16 > rb)
+            // Source rows; padding rows past nvalid read row 0 (their outputs are not stored),
+            // rows with an invalid pair id are zero-filled.
+            uint32_t rowv[32];
+            uint32_t bad = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int r = rb + 8 * i;
+                uint32_t row = 0;
+                if (r < nvalid) {
+                    if (p.per_pair) {
+                        row = (uint32_t)(i0 + r);
+                    } else {
+                        const int f = __ldg(p.perm + i0 + r);
+                        if (f < 0 || f >= p.P) {
+                            bad |= 1u << i;
+                            if (p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+                        } else {
+                            row = (uint32_t)(f / p.k);
+                        }
+                    }
+                }
+                rowv[i] = row;
+            }
+            int prev_s = -1;
+            for (int kc = 0; kc < nk; ++kc, ++it) {
+                const int s = it % kStagesB;
+                if (!mbar_wait(emptyB + s, ((it / kStagesB) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const uint32_t dst = smem_u32(sB + s * kBBytes) + rb * 128 + ((q ^ rb) << 4);
+                const uint8_t* g = xq + (size_t)kc * (kBK * 2);
+                if (bad == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < cnt) cp_async16(dst + i * 1024, g + (size_t)rowv[i] * pitch, 16u);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < cnt) cp_async16(dst + i * 1024, g + (size_t)rowv[i] * pitch, (bad >> i) & 1 ? 0u : 16u);
+                }
+                cp_async_commit();
+                if (prev_s >= 0) {
+                    cp_async_wait<1>();
+                    fence_async_smem();
+                    mbar_arrive(fullB + prev_s);
+                }
+                prev_s = s;
+            }
+            cp_async_wait<0>();
+            fence_async_smem();
+            if (ok && prev_s >= 0) mbar_arrive(fullB + prev_s);
+        }
+        cp_async_wait<0>();
+    } else if (warp < kFirstDec2) {
+        // ------------------------------------------------ scale block and code chunks
+        const int nsw = ngroups >> 1;  // scale words per row (ngroups even, at most 64)
+        const uint32_t sS0 = smem_u32(sS), sC0 = smem_u32(sC);
+        uint32_t cc = 0, tile_it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
+            int e, mt, nt, i0, nvalid;
+            item_coords(item, e, mt, nt, i0, nvalid);
+            const int m0 = mt * kBM;
+            if (!mbar_wait(sempty, (tile_it & 1) ^ 1, abort_flag)) { ok = false; break; }
+            const uint32_t* sbase =
+                reinterpret_cast<const uint32_t*>(p.scales + (int64_t)e * p.ess + (int64_t)m0 * ngroups);
+            if (lane < nsw) {
+                for (int r = 0; r < kBM; ++r)
+                    cp_async4(sS0 + r * 128 + ((lane ^ (r & 31)) << 2), sbase + (int64_t)r * nsw + lane, 4u);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            mbar_arrive(sfull);
+            const uint32_t* cbase = p.codes + (int64_t)e * p.esw + (int64_t)m0 * p.row_stride;
+            for (int c = 0; c < nchunks; ++c, ++cc) {
+                const int slot = cc % kChunkSlots;
+                if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const uint32_t dst = sC0 + slot * kChunkBytes;
+                const int64_t gw = (int64_t)c * 32 + lane;
+                const bool in = gw < p.row_stride;  // words past the padded row read as zero
+                const uint32_t* src = cbase + (in ? gw : 0);
+                for (int r = 0; r < kBM; ++r)
+                    cp_async4(dst + r * 128 + ((lane ^ (r & 31)) << 2), src + (int64_t)r * p.row_stride,
+                              in ? 4u : 0u);
+                cp_async_commit();
+                cp_async_wait<0>();
+                mbar_arrive(cfull + slot);
+            }
+        }
+        cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------ decoders, then epilogue
+        const int dw = warp - kFirstDec2;  // 0..15
+        const int grp = dw >> 3;           // takes the stages with it & 1 == grp
+        const int h = (dw >> 2) & 1;       // which 32 codes of the 64-wide stage
+        const int part = dw >> 2;          // row-max quarter; epilogue column quarter
+        const int r = (dw & 3) * 32 + lane;
+        const int quarter = warp & 3;      // TMEM lanes this warp may access (== dw & 3)
+        const uint32_t lutl = smem_u32(lut) + (COPIES == 32 ? lane * 4 : 0);
+        const uint32_t srow = smem_u32(sS) + r * 128 + ((r & 31) << 2);  // word w of the row: srow ^ (w << 2)
+        const uint32_t crow0 = smem_u32(sC) + r * 128 + ((r & 31) << 2);
+        const uint32_t arow0 = smem_u32(sA) + r * 128 + ((r & 7) << 4);  // 16-byte piece c: arow ^ (c << 4)
+        uint32_t it = 0, tile_it = 0, dec_phase = 0, cc = 0;
+        bool ok = true;
+        auto dec_sync = [&]() -> bool {
+            mbar_arrive(decbar);
+            const bool rr = mbar_wait(decbar, dec_phase, abort_flag);
+            dec_phase ^= 1;
+            return rr;
+        };
+        auto scale_at = [&](int g) -> float {
+            return half_bits_to_float((uint16_t)lds16((srow ^ ((g >> 1) << 2)) + (g & 1) * 2));
+        };
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
+            int e, mt, nt, i0, nvalid;
+            item_coords(item, e, mt, nt, i0, nvalid);
+            const int m0 = mt * kBM;
+            if (!mbar_wait(sfull, tile_it & 1, abort_flag)) { ok = false; break; }
+            float mx = 0.f;
+            for (int g = part; g < ngroups; g += 4) mx = fmaxf(mx, scale_at(g));
+            rowmax_part[part * kBM + r] = mx;
+            if (!dec_sync()) { ok = false; break; }
+            float smax = fmaxf(fmaxf(rowmax_part[r], rowmax_part[kBM + r]),
+                               fmaxf(rowmax_part[2 * kBM + r], rowmax_part[3 * kBM + r]));
+            if (!(smax > 0.f)) smax = 1.f;
+            const float inv = 1.0f / smax;
+            if (part == 0) rowscale[r] = smax;
+            uint32_t crow = crow0;
+            int sub = 0;
+            for (int kc = 0; kc < nk && ok; ++kc, ++it) {
+                if (sub == 0) {
+                    const int slot = cc % kChunkSlots;
+                    if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
+                    crow = crow0 + slot * kChunkBytes;
+                }
+                if ((int)(it & 1) == grp) {
+                    const int s = it % kStagesA;
+                    if (!mbar_wait(emptyA + s, ((it / kStagesA) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    const int lq = 64 * sub + 32 * h;  // first code of this thread within the chunk
+                    const int w0 = lq / F::kCW, pos0 = lq - w0 * F::kCW;
+                    uint32_t W[F::kWords];
+#pragma unroll
+                    for (int j = 0; j < F::kWords; ++j) W[j] = lds32(crow ^ ((w0 + j) << 2));
+                    const int g0 = (kc * kBK + 32 * h) / G;
+                    const float r0 = scale_at(g0) * inv;
+                    const float r1 = G == 16 ? scale_at(g0 + 1) * inv : r0;
+                    const uint32_t rr0 = pack2<XT>(r0, r0), rr1 = pack2<XT>(r1, r1);
+                    uint32_t out[16];
+                    auto dec = [&](auto pos_c) {
+                        constexpr int POS0 = decltype(pos_c)::value;
+                        constexpr uint32_t kMask = (1u << (2 * F::kBits)) - 1u;
+                        constexpr int kStride = COPIES * 4;  // bytes between table entries
+                        constexpr int kLog = COPIES == 32 ? 7 : 2;
+#pragma unroll
+                        for (int pp = 0; pp < 16; ++pp) {
+                            const int tt = POS0 + 2 * pp;
+                            const int sh = F::kBits * (tt % F::kCW);
+                            const uint32_t w = W[tt / F::kCW];
+                            const uint32_t off =
+                                (sh >= kLog ? (w >> (sh - kLog)) : (w << (kLog - sh))) & (kMask * kStride);
+                            out[pp] = hmul2_bits<XT>(lds32(lutl + off), pp < 8 ? rr0 : rr1);
+                        }
+                    };
+                    if constexpr (LEVELS == 8) {
+                        switch (pos0) {
+                            case 0: dec(std::integral_constant<int, 0>{}); break;
+                            case 2: dec(std::integral_constant<int, 2>{}); break;
+                            case 4: dec(std::integral_constant<int, 4>{}); break;
+                            case 6: dec(std::integral_constant<int, 6>{}); break;
+                            default: dec(std::integral_constant<int, 8>{}); break;
+                        }
+                    } else {
+                        dec(std::integral_constant<int, 0>{});
+                    }
+                    const uint32_t arow = arow0 + s * kABytes;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        sts128(arow ^ ((4 * h + c4) << 4), out[4 * c4], out[4 * c4 + 1], out[4 * c4 + 2],
+                               out[4 * c4 + 3]);
+                    fence_async_smem();
+                    mbar_arrive(fullA + s);
+                }
+                if (++sub == SPC || kc == nk - 1) {
+                    mbar_arrive(cempty + cc % kChunkSlots);
+                    ++cc;
+                    sub = 0;
+                }
+            }
+            if (!ok) break;
+            mbar_arrive(sempty);  // scale block no longer read (row scales kept in rowscale)
+            if (!mbar_wait(tile_full, tile_it & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            if (!dec_sync()) { ok = false; break; }
+            const int m = quarter * 32 + lane;
+            const float rs = rowscale[m];
+            for (int c0 = part * 64; c0 < part * 64 + 64; c0 += 32) {
+                if (c0 < nvalid) {
+                    uint32_t v[32];
+                    tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < nvalid)
+                            store_from_float(p.y, (int64_t)(i0 + c0 + j) * p.rows + m0 + m, p.ydt,
+                                             __uint_as_float(v[j]) * rs);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tile_empty);
+        }
+    }
+
+    __syncthreads();
+    if (tid == 0 && *abort_flag && p.err) atomicOr(p.err, TQ_DEVERR_TIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kNT) : "memory");
+    }
+}
+
+size_t qmm2_smem_bytes(int levels, int experts) {
+    const int copies = levels == 16 ? 1 : 32;
+    return 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes + (size_t)kChunkSlots * kChunkBytes +
+           kScaleBlock + (size_t)levels * levels * copies * 4 + 5 * kBM * 4 + 32 * 8 + 32 +
+           (size_t)(experts + 1) * 4;
+}
+
 size_t qmm_smem_bytes(int levels, int experts) {
     return 1024 + (size_t)kStages * (kABytes + kBBytes) + (2 * kStages + 4) * 8 + 32 + (size_t)levels * levels * 8 +
            3 * kBM * 4 + (size_t)(experts + 1) * 4;
@@ -509,9 +959,33 @@ tq_status launch_qmm(const QmmParams& p, cudaStream_t st) {
     return launch_status();
 }
 
+// The staged kernel holds a tile's scale block in 128 bytes per row: it takes
+// an even group count of at most 64 per row; other shapes use the first kernel.
+bool staged_fits(const QmmParams& p, int G, int levels) {
+    const int ngroups = p.cols / G;
+    return ngroups <= 64 && ngroups % 2 == 0 && p.ess % 2 == 0 && aligned(p.scales, 4) &&
+           qmm2_smem_bytes(levels, p.experts) <= 227 * 1024;
+}
+
+template <int LEVELS, int G, int XT>
+tq_status launch_qmm2(const QmmParams& p, cudaStream_t st) {
+    const size_t smem = qmm2_smem_bytes(LEVELS, p.experts);
+    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, XT>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    gather_qmm2_kernel<LEVELS, G, XT><<<sms > 0 ? sms : 148, kThreads2, smem, st>>>(p);
+    return launch_status();
+}
+
+template <int LEVELS, int G, int XT>
+tq_status launch_any(const QmmParams& p, cudaStream_t st) {
+    return staged_fits(p, G, LEVELS) ? launch_qmm2<LEVELS, G, XT>(p, st) : launch_qmm<LEVELS, G, XT>(p, st);
+}
+
 template <int LEVELS, int G>
 tq_status dispatch_xt(const QmmParams& p, int xt, cudaStream_t st) {
-    return xt == 0 ? launch_qmm<LEVELS, G, 0>(p, st) : launch_qmm<LEVELS, G, 1>(p, st);
+    return xt == 0 ? launch_any<LEVELS, G, 0>(p, st) : launch_any<LEVELS, G, 1>(p, st);
 }
 
 template <int LEVELS>
