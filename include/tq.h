@@ -226,14 +226,17 @@ tq_status tq_moe_combine(const float* y, const float* probs, const int32_t* pair
  *   sorted pairs' own inputs).
  * Codes are decoded to the operand type xdt (f16 or bf16) in shared memory and
  * multiplied with fp32 accumulation.  x: device [T or P, cols] of xdt (already
- * rotated).  perm: device int32 [P] (ignored when per_pair_input);
- * offsets: device int32 [experts+1].  y: device [P, rows] of ydt (f32 or
- * bf16).  ws: device scratch of tq_gather_qmm_workspace_bytes(experts) bytes.
+ * rotated, 16-byte aligned).  perm: device int32 [P] (ignored when
+ * per_pair_input); an entry outside [0, P) sets TQ_DEVERR_BAD_ID and its pair
+ * reads a zero input row.  offsets: device int32 [experts+1].  y: device
+ * [P, rows] of ydt (f32 or bf16).  ws: 16-byte aligned device scratch of at
+ * least tq_gather_qmm_workspace_bytes(P, cols, per_pair_input) bytes (the
+ * token rows gathered into sorted pair order; TQ_ERR_INVALID if smaller).
  * cols must be a multiple of 64, rows a multiple of 128. */
 tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtype xdt, const int32_t* perm,
                         const int32_t* offsets, int32_t P, int32_t k, int32_t per_pair_input,
                         void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
-size_t tq_gather_qmm_workspace_bytes(int32_t experts);
+size_t tq_gather_qmm_workspace_bytes(int32_t P, int32_t cols, int32_t per_pair_input);
 
 /* Dequantize selected experts to dense rotated-domain weights, for a regular matmul.
  * "How it works", row "Anything else" (polar_dequant_experts).

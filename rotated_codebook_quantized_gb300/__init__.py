@@ -62,7 +62,7 @@ _SIGS = {
     "tq_moe_combine": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _i32, _c_p]),
     "tq_gather_qmm": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _i32, _i32, _i32, _c_p, _i32, _c_p, _sz,
                              _c_p, _c_p]),
-    "tq_gather_qmm_workspace_bytes": (_sz, [_i32]),
+    "tq_gather_qmm_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "tq_dequant_experts": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
     "tq_kv_quantize": (_i32, [_c_p, _c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t),
                               _P(tq_codebook_t), _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p]),
@@ -322,7 +322,7 @@ def gather_qmm(w: QWeight, x, perm, offsets, k: int, per_pair_input: bool = Fals
     _contig(x, "x")
     P = int(perm.numel()) if not per_pair_input else int(x.shape[0])
     y = torch.empty((P, w.rows), dtype=out_dtype or torch.float32, device=x.device)
-    nb = int(load().tq_gather_qmm_workspace_bytes(w.experts))
+    nb = int(load().tq_gather_qmm_workspace_bytes(P, w.cols, int(per_pair_input)))
     ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=x.device)
     q = w.c()
     _check(load().tq_gather_qmm(ctypes.byref(q), _ptr(x), _dt(x), _ptr(perm), _ptr(offsets), P, k,

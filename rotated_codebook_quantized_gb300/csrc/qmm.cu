@@ -20,6 +20,8 @@
 // (expert, 128-row tile, 256-pair tile) in expert-major order so that CTAs
 // running together share the expert's codes in L2.  Every wait on an mbarrier
 // is bounded; on expiry the CTA sets TQ_DEVERR_TIMEOUT, drains and frees TMEM.
+#include <cudaTypedefs.h>
+
 #include <type_traits>
 
 #include "common.cuh"
@@ -53,12 +55,15 @@ TQ_DEVFN void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 
+// The waiting thread is suspended (issuing nothing) until the phase completes
+// or about kSuspendNs elapse, so idle roles leave the issue slots to the others.
+constexpr uint32_t kSuspendNs = 20000;
 TQ_DEVFN bool mbar_try_wait(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
+        : "r"(smem_u32(b)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -74,7 +79,18 @@ TQ_DEVFN bool mbar_wait_drain(uint64_t* b, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // (and raises the CTA's abort flag) if it did not within kWaitCycles or if
 // another role already aborted.
+TQ_DEVFN bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_test(b, parity)) return true;  // common case first: no clock read, no suspension
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
         if (*abort_flag) return false;
@@ -134,6 +150,15 @@ TQ_DEVFN void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : TQ_R8(0), TQ_R8(8), TQ_R8(16), TQ_R8(24)
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+TQ_DEVFN void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : TQ_R8(0), TQ_R8(8)
         : "r"(taddr)
         : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -496,34 +521,78 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
 
 // ---------------------------------------------------------------- staged variant
 //
-// Same contraction and tile walk as gather_qmm_kernel, with the data movement
-// reorganised so that neither the copies nor the decode starve the tensor core:
-//   warp 0      issues the MMAs (one thread);
-//   warps 1-2   gather the pairs' input rows: each thread keeps the source row
-//               indices of its 32 rows in registers for the whole tile and
-//               issues one 16-byte cp.async per row and stage, 8 lanes per
-//               128-byte row segment (3-stage ring of 256 x 64 operand tiles);
-//   warp 3      stages the m-tile's scale block and its packed codes, 32 words
-//               (128 bytes) per row and chunk, in a 2-slot ring; word w of row r
-//               is stored at word w ^ (r & 31) of the row so that the decoders'
-//               reads (one word of 32 consecutive rows) are free of bank conflicts;
-//   warps 4-19  decode in two groups of 8 warps taking alternate stages: pairs
+// Same contraction and tile walk as gather_qmm_kernel, organised so that the
+// tensor core is fed continuously across tiles:
+//   warps 0-1   issue the MMAs (one thread each, sharing each tile) into one of
+//               two TMEM accumulators (2 x 256 columns), so that the next tile's
+//               MMAs run while the previous accumulator is drained;
+//   warps 2-3   load B stages, alternately, each with one 2-D tensor copy
+//               (128-byte swizzle) of the pairs' input rows, which are
+//               contiguous in sorted order (token rows are gathered into that
+//               order by a first pass).  A thread is blocked for a few hundred
+//               cycles by each copy it issues, hence one copy per stage and two
+//               issuing warps;
+//   warp 4      loads the m-tile's packed codes, 32 words of 128 rows per
+//               chunk, with one 3-D tensor copy (128-byte swizzle) into a
+//               2-slot ring;
+//   warp 5      copies the scales those codes need into the same slot
+//               (cp.async, SW words per row, SW a power of two; word j of row
+//               r stored at j ^ ((r / (32 / SW)) % SW) so that one group read
+//               across 32 rows hits 32 banks);
+//   warps 6-21  decode in two groups of 8 warps taking alternate stages: pairs
 //               of codes index a per-lane copy of a table of packed operand
-//               pairs and one half2 multiply applies s_group / s_rowmax; then
-//               all 16 drain the accumulator (epilogue).
-constexpr int kStagesA = 4, kStagesB = 3, kChunkSlots = 2;
-constexpr int kChunkBytes = kBM * 128;   // 32 code words of each of the 128 rows
-constexpr int kScaleBlock = kBM * 128;   // up to 64 fp16 scales of each row
-constexpr int kDec2 = 16;                // decoder warps
-constexpr int kFirstDec2 = 4;
-constexpr int kThreads2 = 32 * (kFirstDec2 + kDec2);
+//               pairs and one half2 multiply applies the group scale, so the
+//               operand is c[code] * s_group in the operand type;
+//   warps 22-25 drain the accumulators (epilogue).
+constexpr int kChunkSlots = 2;
+constexpr int kChunkCodeBytes = kBM * 128;            // 32 code words of each of the 128 rows
+constexpr int kDec2 = 16;                             // decoder warps
+constexpr int kMmaWarps = 2;                          // MMA issuers (warps 0, 1)
+constexpr int kBWarps = 2;                            // B producers (warps 2, 3)
+constexpr int kCodeWarp = kMmaWarps + kBWarps, kScaleWarp = kCodeWarp + 1;
+constexpr int kFirstDec2 = kScaleWarp + 1;
+constexpr int kEpiWarps = 4;
+constexpr int kFirstEpi = kFirstDec2 + kDec2;
+constexpr int kThreads2 = 32 * (kFirstEpi + kEpiWarps);
 constexpr int kDecThreads2 = 32 * kDec2;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kBoxRows[5] = {256, 128, 64, 32, 16};  // host side; the kernel uses 256 >> i
 
-template <int LEVELS>
+struct QmmMaps {
+    CUtensorMap b[5];  // pair rows, boxes of 64 columns x kBoxRows[i] rows
+    CUtensorMap c;     // codes [experts][rows][row_stride] words, box 32 x 128 x 1
+};
+
+// Most scale words (pairs of fp16 group scales) one row of a code chunk needs.
+constexpr int chunk_scale_words(int cpc, int g) {
+    int most = 0;
+    for (int c = 0; c <= 2 * g; ++c) {
+        const int w = (((c + 1) * cpc - 1) / g >> 1) - ((c * cpc / g) >> 1) + 1;
+        most = w > most ? w : most;
+    }
+    return most;
+}
+constexpr int pow2_at_least(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <int LEVELS, int G>
 struct Q2Fmt {
     using F = BitFmt<LEVELS>;
     static constexpr int kSPC = F::kCW / 2;                    // stages (64 codes) per 32-word chunk
+    static constexpr int kCPC = 32 * F::kCW;                   // codes per chunk
     static constexpr int kLutCopies = LEVELS == 16 ? 1 : 32;  // per-lane copies when small enough
+    static constexpr int kLutBytes = LEVELS * LEVELS * kLutCopies * 4;
+    static constexpr int kSW = pow2_at_least(chunk_scale_words(kCPC, G));  // scale words per row in a slot
+    static constexpr int kChunkBytes = kChunkCodeBytes + kBM * kSW * 4;
+    // A and B stages share one ring (one full and one empty barrier per stage, so the MMA
+    // thread waits once and commits once per stage).
+    static constexpr int kStages = 3;
+    static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + kChunkSlots * kChunkBytes + kLutBytes + 64 * 8 +
+                                 32;  // plus 8 * (experts + 1)
+    static_assert(kSW <= 16, "scale words per chunk row");
 };
 
 template <int XT>
@@ -538,9 +607,25 @@ TQ_DEVFN uint32_t hmul2_bits(uint32_t a, uint32_t b) {
     }
 }
 
+// fp16 scale bits -> the operand type, in both halves of a word.
+template <int XT>
+TQ_DEVFN uint32_t scale_pair(uint32_t hbits) {
+    if constexpr (XT == 0) {
+        return hbits | (hbits << 16);
+    } else {
+        const float f = half_bits_to_float((uint16_t)hbits);
+        return pack2<1>(f, f);
+    }
+}
+
 TQ_DEVFN uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+TQ_DEVFN uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
 }
 TQ_DEVFN uint32_t lds16(uint32_t a) {
@@ -554,39 +639,53 @@ TQ_DEVFN void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
 TQ_DEVFN void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
+TQ_DEVFN void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+TQ_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+TQ_DEVFN void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
 
 template <int LEVELS, int G, int XT>
-__global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmParams p) {
+__global__ void __launch_bounds__(kThreads2, 1)
+    gather_qmm2_kernel(const QmmParams p, const __grid_constant__ QmmMaps tm) {
     using F = BitFmt<LEVELS>;
-    using Q = Q2Fmt<LEVELS>;
-    constexpr int SPC = Q::kSPC, NL = LEVELS * LEVELS, COPIES = Q::kLutCopies;
+    using Q = Q2Fmt<LEVELS, G>;
+    constexpr int SPC = Q::kSPC, CPC = Q::kCPC, NL = LEVELS * LEVELS, COPIES = Q::kLutCopies;
+    constexpr int kStages = Q::kStages, kChunkBytes = Q::kChunkBytes, SW = Q::kSW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = base;                                      // [4][128 x 64]
-    uint8_t* sB = sA + kStagesA * kABytes;                   // [3][256 x 64]
-    uint8_t* sC = sB + kStagesB * kBBytes;                   // [2][128 rows x 128 B] code chunks
-    uint8_t* sS = sC + kChunkSlots * kChunkBytes;            // [128 rows x 128 B] scale block
-    uint32_t* lut = reinterpret_cast<uint32_t*>(sS + kScaleBlock);       // [NL][COPIES] operand pairs
-    float* rowscale = reinterpret_cast<float*>(lut + NL * COPIES);       // [128]
-    float* rowmax_part = rowscale + kBM;                                 // [4][128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(rowmax_part + 4 * kBM);
-    uint64_t* fullA = bars;
-    uint64_t* emptyA = fullA + kStagesA;
-    uint64_t* fullB = emptyA + kStagesA;
-    uint64_t* emptyB = fullB + kStagesB;
-    uint64_t* cfull = emptyB + kStagesB;
+    uint8_t* sA = base;                                      // [kStages][128 x 64]
+    uint8_t* sB = sA + kStages * kABytes;                    // [kStages][256 x 64]
+    uint8_t* sC = sB + kStages * kBBytes;                    // [2] x (codes 128 x 128 B, scales 128 x SW words)
+    uint32_t* lut = reinterpret_cast<uint32_t*>(sC + kChunkSlots * kChunkBytes);  // [NL][COPIES] operand pairs
+    uint64_t* bars = reinterpret_cast<uint64_t*>(lut + NL * COPIES);
+    // full[s]: stage s's A (its decoder group) and B (the copy's bytes) are in place;
+    // empty[s]: the MMAs that read stage s have completed.
+    uint64_t* full = bars;
+    uint64_t* empty = full + kStages;
+    uint64_t* cfull = empty + kStages;
     uint64_t* cempty = cfull + kChunkSlots;
-    uint64_t* sfull = cempty + kChunkSlots;
-    uint64_t* sempty = sfull + 1;
-    uint64_t* tile_full = sempty + 1;
-    uint64_t* tile_empty = tile_full + 1;
-    uint64_t* drain = tile_empty + 1;
-    uint64_t* decbar = drain + 1;
-    int* ctl = reinterpret_cast<int*>(decbar + 1);
+    uint64_t* tile_full = cempty + kChunkSlots;  // [2]
+    uint64_t* tile_empty = tile_full + 2;        // [2]
+    uint64_t* drain = tile_empty + 2;
+    int* ctl = reinterpret_cast<int*>(drain + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl);
     volatile int* abort_flag = ctl + 1;
     int* total_items = ctl + 2;
-    int* cum = ctl + 8;  // [experts + 1]
+    int* cum = ctl + 8;              // [experts + 1]
+    int* offs = cum + (p.experts + 1);  // [experts + 1] pair offsets
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.experts;
@@ -595,7 +694,7 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
     const int ngroups = p.cols / G;
     const int nchunks = (nk + SPC - 1) / SPC;
 
-    for (int i = tid; i <= E; i += kThreads2) cum[i] = p.offsets[i];
+    for (int i = tid; i <= E; i += kThreads2) cum[i] = offs[i] = p.offsets[i];
     for (int i = tid; i < NL * COPIES; i += kThreads2) {
         const int idx = i / COPIES;
         lut[i] = pack2<XT>(p.centroids[idx & (LEVELS - 1)], p.centroids[idx / LEVELS]);
@@ -618,24 +717,19 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
         cum[E] = acc;
         *total_items = ok ? acc : -1;
         *abort_flag = 0;
-        for (int s = 0; s < kStagesA; ++s) {
-            mbar_init(fullA + s, 32 * kDec2 / 2);
-            mbar_init(emptyA + s, 1);
-        }
-        for (int s = 0; s < kStagesB; ++s) {
-            mbar_init(fullB + s, 64);
-            mbar_init(emptyB + s, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full + s, 32 * kDec2 / 2 + 1);  // a decoder group + the B copy
+            mbar_init(empty + s, kMmaWarps);          // a commit from each MMA thread
         }
         for (int s = 0; s < kChunkSlots; ++s) {
-            mbar_init(cfull + s, 32);
+            mbar_init(cfull + s, 1 + 32);  // the code copy's arrival and the 32 scale lanes
             mbar_init(cempty + s, kDecThreads2);
         }
-        mbar_init(sfull, 32);
-        mbar_init(sempty, kDecThreads2);
-        mbar_init(tile_full, 1);
-        mbar_init(tile_empty, kDecThreads2);
-        mbar_init(drain, 1);
-        mbar_init(decbar, kDecThreads2);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tile_full + b, kMmaWarps);
+            mbar_init(tile_empty + b, 32 * kEpiWarps);
+        }
+        mbar_init(drain, kMmaWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -646,7 +740,7 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kNT)
+                     "r"(2 * kNT)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -662,7 +756,7 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
             if (cum[mid] <= item) lo = mid; else hi = mid - 1;
         }
         e = lo;
-        const int off0 = p.offsets[e], n = p.offsets[e + 1] - off0;
+        const int off0 = offs[e], n = offs[e + 1] - off0;
         const int ntiles = (n + kNT - 1) / kNT;
         const int local = item - cum[e];
         mt = local / ntiles;
@@ -671,200 +765,182 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
         nvalid = min(kNT, n - nt * kNT);
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------ MMA issuer
+    if (warp < kMmaWarps) {
+        // ------------------------------------------------ MMA issuers (one thread each)
+        // Each MMA instruction blocks its thread for tens of cycles and each commit for about a
+        // hundred, so two threads share a tile: with at most 128 pairs they take alternate
+        // K stages into their own 128 accumulator columns (the epilogue adds the two); with
+        // more, thread 0 computes pair columns 0..127 and thread 1 the rest.  Both wait for
+        // every stage and commit every stage, so a slot is released only after both.
         if (lane == 0) {
+            const int me = warp;
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
             uint32_t it = 0, tile_it = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
                 int e, mt, nt, i0, nvalid;
                 item_coords(item, e, mt, nt, i0, nvalid);
-                const uint32_t idesc = f16_idesc(XT, (nvalid + 15) & ~15);
-                if (!mbar_wait(tile_empty, (tile_it & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const int ninst = (nvalid + 15) & ~15;
+                const bool ksplit = ninst <= 128 && nk >= 2;
+                const int ncols = ksplit ? ninst : (me == 0 ? min(ninst, 128) : ninst - 128);
+                const uint32_t idesc = f16_idesc(XT, ncols > 0 ? ncols : 16);
+                const int buf = tile_it & 1;
+                if (!mbar_wait(tile_empty + buf, ((tile_it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * kNT + me * 128);
+                const uint32_t boff = ksplit ? 0u : (uint32_t)(me * 128 * 128);  // B rows of thread 1's columns
                 for (int kc = 0; kc < nk; ++kc, ++it) {
-                    const int sa = it % kStagesA, sb = it % kStagesB;
-                    if (!mbar_wait(fullA + sa, (it / kStagesA) & 1, abort_flag) ||
-                        !mbar_wait(fullB + sb, (it / kStagesB) & 1, abort_flag)) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint64_t ad = sw128_desc(a0 + sa * kABytes), bd = sw128_desc(b0 + sb * kBBytes);
+                    const bool mine = ksplit ? (kc & 1) == me : ncols > 0;
+                    if (mine) {
+                        const bool first = ksplit ? kc == me : kc == 0;
+                        const uint64_t ad = sw128_desc(a0 + s * kABytes), bd = sw128_desc(b0 + s * kBBytes + boff);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kc | kk) != 0);
-                    tc_commit(emptyA + sa);
-                    tc_commit(emptyB + sb);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc_mma(d, ad + 2 * kk, bd + 2 * kk, idesc, !(first && kk == 0));
+                    }
+                    tc_commit(empty + s);
                 }
                 if (!ok) break;
-                tc_commit(tile_full);
+                tc_commit(tile_full + buf);
             }
             tc_commit(drain);
             if (!mbar_wait_drain(drain, 0)) *abort_flag = 1;
         }
         __syncwarp();
-    } else if (warp < 3) {
-        // ------------------------------------------------ B producers: rows rb + 8 i of every stage
-        const int t = tid - 32;            // 0..63
-        const int q = t & 7, rb = t >> 3;  // 16-byte piece; first row (rows rb + 8 i share r & 7 == rb)
-        const uint8_t* xq = reinterpret_cast<const uint8_t*>(p.x) + q * 16;
-        const uint32_t pitch = (uint32_t)p.cols * 2u;
-        uint32_t it = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-            int e, mt, nt, i0, nvalid;
-            item_coords(item, e, mt, nt, i0, nvalid);
-            const int ninst = (nvalid + 15) & ~15;
-            const int cnt = (ninst - rb + 7) >> 3;  // my rows below ninst (ninst >= 16 > rb)
-            // Source rows; padding rows past nvalid read row 0 (their outputs are not stored),
-            // rows with an invalid pair id are zero-filled.
-            uint32_t rowv[32];
-            uint32_t bad = 0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = rb + 8 * i;
-                uint32_t row = 0;
-                if (r < nvalid) {
-                    if (p.per_pair) {
-                        row = (uint32_t)(i0 + r);
-                    } else {
-                        const int f = __ldg(p.perm + i0 + r);
-                        if (f < 0 || f >= p.P) {
-                            bad |= 1u << i;
-                            if (p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
-                        } else {
-                            row = (uint32_t)(f / p.k);
-                        }
-                    }
+    } else if (warp < kMmaWarps + kBWarps) {
+        // ------------------------------------------------ B: one tensor copy per stage, warps alternate stages
+        if (lane == 0) {
+            const int bw = warp - kMmaWarps;
+            const uint32_t b0 = smem_u32(sB);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                int e, mt, nt, i0, nvalid;
+                item_coords(item, e, mt, nt, i0, nvalid);
+                int bi = 0;
+                while (bi < 4 && (128 >> bi) >= nvalid) ++bi;  // smallest box of 256 >> bi rows >= nvalid
+                const int box_rows = 256 >> bi;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    if ((int)(it % kBWarps) != bw) continue;
+                    const int s = it % kStages;
+                    if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    uint64_t* fb = full + s;
+                    mbar_expect_tx(fb, (uint32_t)box_rows * 128u);
+                    tma_load_2d(b0 + s * kBBytes, &tm.b[bi], kc * kBK, i0, fb);
                 }
-                rowv[i] = row;
             }
-            int prev_s = -1;
-            for (int kc = 0; kc < nk; ++kc, ++it) {
-                const int s = it % kStagesB;
-                if (!mbar_wait(emptyB + s, ((it / kStagesB) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                const uint32_t dst = smem_u32(sB + s * kBBytes) + rb * 128 + ((q ^ rb) << 4);
-                const uint8_t* g = xq + (size_t)kc * (kBK * 2);
-                if (bad == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < cnt) cp_async16(dst + i * 1024, g + (size_t)rowv[i] * pitch, 16u);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < cnt) cp_async16(dst + i * 1024, g + (size_t)rowv[i] * pitch, (bad >> i) & 1 ? 0u : 16u);
-                }
-                cp_async_commit();
-                if (prev_s >= 0) {
-                    cp_async_wait<1>();
-                    fence_async_smem();
-                    mbar_arrive(fullB + prev_s);
-                }
-                prev_s = s;
-            }
-            cp_async_wait<0>();
-            fence_async_smem();
-            if (ok && prev_s >= 0) mbar_arrive(fullB + prev_s);
+            // copies this thread issued that may still be in flight complete before the CTA may exit
+            // (the full barrier also waits for the decoders' arrivals, which come unless they aborted)
+            for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
+                if ((int)(j % kBWarps) == bw && !mbar_wait_drain(full + j % kStages, (j / kStages) & 1))
+                    *abort_flag = 1;
         }
-        cp_async_wait<0>();
-    } else if (warp < kFirstDec2) {
-        // ------------------------------------------------ scale block and code chunks
-        const int nsw = ngroups >> 1;  // scale words per row (ngroups even, at most 64)
-        const uint32_t sS0 = smem_u32(sS), sC0 = smem_u32(sC);
-        uint32_t cc = 0, tile_it = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
+        __syncwarp();
+    } else if (warp == kCodeWarp) {
+        // ------------------------------------------------ code chunks: one tensor copy each
+        if (lane == 0) {
+            const uint32_t c0 = smem_u32(sC);
+            uint32_t cc = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                int e, mt, nt, i0, nvalid;
+                item_coords(item, e, mt, nt, i0, nvalid);
+                for (int c = 0; c < nchunks; ++c, ++cc) {
+                    const int slot = cc % kChunkSlots;
+                    if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(cfull + slot, (uint32_t)kChunkCodeBytes);
+                    tma_load_3d(c0 + slot * kChunkBytes, &tm.c, c * 32, mt * kBM, e, cfull + slot);
+                }
+            }
+            for (uint32_t j = cc > (uint32_t)kChunkSlots ? cc - kChunkSlots : 0; j < cc; ++j) {
+                // the slot's phase also waits for the scale lanes: wait on the copy's bytes alone is not
+                // possible, so wait for the phase (the scale lanes arrive unless they aborted)
+                if (!mbar_wait_drain(cfull + j % kChunkSlots, (j / kChunkSlots) & 1)) *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == kScaleWarp) {
+        // ------------------------------------------------ the scales of each code chunk
+        const uint32_t* sc32 = reinterpret_cast<const uint32_t*>(p.scales);  // ngroups and ess are even
+        const int nsw_row = ngroups >> 1;
+        uint32_t cc = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
             int e, mt, nt, i0, nvalid;
             item_coords(item, e, mt, nt, i0, nvalid);
-            const int m0 = mt * kBM;
-            if (!mbar_wait(sempty, (tile_it & 1) ^ 1, abort_flag)) { ok = false; break; }
-            const uint32_t* sbase =
-                reinterpret_cast<const uint32_t*>(p.scales + (int64_t)e * p.ess + (int64_t)m0 * ngroups);
-            if (lane < nsw) {
-                for (int r = 0; r < kBM; ++r)
-                    cp_async4(sS0 + r * 128 + ((lane ^ (r & 31)) << 2), sbase + (int64_t)r * nsw + lane, 4u);
-            }
-            cp_async_commit();
-            cp_async_wait<0>();
-            mbar_arrive(sfull);
-            const uint32_t* cbase = p.codes + (int64_t)e * p.esw + (int64_t)m0 * p.row_stride;
+            const uint32_t* rows0 = sc32 + ((int64_t)e * p.ess + (int64_t)mt * kBM * ngroups) / 2;
+            bool ok = true;
             for (int c = 0; c < nchunks; ++c, ++cc) {
                 const int slot = cc % kChunkSlots;
                 if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                const uint32_t dst = sC0 + slot * kChunkBytes;
-                const int64_t gw = (int64_t)c * 32 + lane;
-                const bool in = gw < p.row_stride;  // words past the padded row read as zero
-                const uint32_t* src = cbase + (in ? gw : 0);
-                for (int r = 0; r < kBM; ++r)
-                    cp_async4(dst + r * 128 + ((lane ^ (r & 31)) << 2), src + (int64_t)r * p.row_stride,
-                              in ? 4u : 0u);
+                const int wlo = (c * CPC / G) >> 1;
+                const int ghi = min(ngroups - 1, ((c + 1) * CPC - 1) / G);
+                const int nw = (ghi >> 1) - wlo + 1;  // 1..SW words per row
+                const int rpi = 32 / nw;              // rows per instruction
+                const int rr = lane / nw, j = lane - rr * nw;
+                const uint32_t dst0 = smem_u32(sC) + slot * kChunkBytes + kChunkCodeBytes;
+                if (rr < rpi) {
+                    for (int r = rr; r < kBM; r += rpi)
+                        cp_async4(dst0 + r * (SW * 4) + ((j ^ ((r / (32 / SW)) & (SW - 1))) << 2),
+                                  rows0 + (int64_t)r * nsw_row + wlo + j, 4u);
+                }
                 cp_async_commit();
                 cp_async_wait<0>();
                 mbar_arrive(cfull + slot);
             }
+            if (!ok) break;
         }
         cp_async_wait<0>();
-    } else {
-        // ------------------------------------------------ decoders, then epilogue
+    } else if (warp < kFirstEpi) {
+        // ------------------------------------------------ decoders
         const int dw = warp - kFirstDec2;  // 0..15
         const int grp = dw >> 3;           // takes the stages with it & 1 == grp
         const int h = (dw >> 2) & 1;       // which 32 codes of the 64-wide stage
-        const int part = dw >> 2;          // row-max quarter; epilogue column quarter
         const int r = (dw & 3) * 32 + lane;
-        const int quarter = warp & 3;      // TMEM lanes this warp may access (== dw & 3)
+        const int rx = r & 7;
         const uint32_t lutl = smem_u32(lut) + (COPIES == 32 ? lane * 4 : 0);
-        const uint32_t srow = smem_u32(sS) + r * 128 + ((r & 31) << 2);  // word w of the row: srow ^ (w << 2)
-        const uint32_t crow0 = smem_u32(sC) + r * 128 + ((r & 31) << 2);
-        const uint32_t arow0 = smem_u32(sA) + r * 128 + ((r & 7) << 4);  // 16-byte piece c: arow ^ (c << 4)
-        uint32_t it = 0, tile_it = 0, dec_phase = 0, cc = 0;
+        const uint32_t crow0 = smem_u32(sC) + r * 128;  // 16-byte piece q of the row: crow + ((q ^ rx) << 4)
+        const uint32_t srow0 = smem_u32(sC) + kChunkCodeBytes + r * (SW * 4);  // word j: srow + ((j ^ sx) << 2)
+        const int sx = (r / (32 / SW)) & (SW - 1);
+        const uint32_t arow0 = smem_u32(sA) + r * 128 + (rx << 4);  // piece q of the A row: arow ^ (q << 4)
+        uint32_t it = 0, cc = 0;
         bool ok = true;
-        auto dec_sync = [&]() -> bool {
-            mbar_arrive(decbar);
-            const bool rr = mbar_wait(decbar, dec_phase, abort_flag);
-            dec_phase ^= 1;
-            return rr;
-        };
-        auto scale_at = [&](int g) -> float {
-            return half_bits_to_float((uint16_t)lds16((srow ^ ((g >> 1) << 2)) + (g & 1) * 2));
-        };
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
-            int e, mt, nt, i0, nvalid;
-            item_coords(item, e, mt, nt, i0, nvalid);
-            const int m0 = mt * kBM;
-            if (!mbar_wait(sfull, tile_it & 1, abort_flag)) { ok = false; break; }
-            float mx = 0.f;
-            for (int g = part; g < ngroups; g += 4) mx = fmaxf(mx, scale_at(g));
-            rowmax_part[part * kBM + r] = mx;
-            if (!dec_sync()) { ok = false; break; }
-            float smax = fmaxf(fmaxf(rowmax_part[r], rowmax_part[kBM + r]),
-                               fmaxf(rowmax_part[2 * kBM + r], rowmax_part[3 * kBM + r]));
-            if (!(smax > 0.f)) smax = 1.f;
-            const float inv = 1.0f / smax;
-            if (part == 0) rowscale[r] = smax;
-            uint32_t crow = crow0;
-            int sub = 0;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            uint32_t crow = crow0, srow = srow0;
+            int sub = 0, gbase = 0;
             for (int kc = 0; kc < nk && ok; ++kc, ++it) {
                 if (sub == 0) {
                     const int slot = cc % kChunkSlots;
                     if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
                     crow = crow0 + slot * kChunkBytes;
+                    srow = srow0 + slot * kChunkBytes;
+                    gbase = ((kc / SPC) * CPC / G) & ~1;  // group at word 0 of the chunk's scale rows
                 }
                 if ((int)(it & 1) == grp) {
-                    const int s = it % kStagesA;
-                    if (!mbar_wait(emptyA + s, ((it / kStagesA) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    const int s = it % kStages;
+                    if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     const int lq = 64 * sub + 32 * h;  // first code of this thread within the chunk
                     const int w0 = lq / F::kCW, pos0 = lq - w0 * F::kCW;
-                    uint32_t W[F::kWords];
-#pragma unroll
-                    for (int j = 0; j < F::kWords; ++j) W[j] = lds32(crow ^ ((w0 + j) << 2));
-                    const int g0 = (kc * kBK + 32 * h) / G;
-                    const float r0 = scale_at(g0) * inv;
-                    const float r1 = G == 16 ? scale_at(g0 + 1) * inv : r0;
-                    const uint32_t rr0 = pack2<XT>(r0, r0), rr1 = pack2<XT>(r1, r1);
+                    const int o = w0 & 3, q0 = w0 >> 2;
+                    // words w0 .. w0 + kWords - 1 lie in pieces q0 and, for 3-bit codes with o != 0, q0 + 1
+                    const uint4 P0 = lds128(crow + ((q0 ^ rx) << 4));
+                    uint4 P1 = P0;
+                    if (F::kBits == 3 && o != 0) P1 = lds128(crow + (((q0 + 1) ^ rx) << 4));
+                    const uint32_t WW[8] = {P0.x, P0.y, P0.z, P0.w, P1.x, P1.y, P1.z, P1.w};
+                    const int g0 = (kc * kBK + 32 * h) / G - gbase;
+                    const uint32_t rr0 = scale_pair<XT>(lds16(srow + (((g0 >> 1) ^ sx) << 2) + (g0 & 1) * 2));
+                    uint32_t rr1 = rr0;
+                    if (G == 16) {
+                        const int g1 = g0 + 1;
+                        rr1 = scale_pair<XT>(lds16(srow + (((g1 >> 1) ^ sx) << 2) + (g1 & 1) * 2));
+                    }
                     uint32_t out[16];
-                    auto dec = [&](auto pos_c) {
-                        constexpr int POS0 = decltype(pos_c)::value;
+                    auto dec = [&](auto pos_c, auto o_c) {
+                        constexpr int POS0 = decltype(pos_c)::value, O = decltype(o_c)::value;
                         constexpr uint32_t kMask = (1u << (2 * F::kBits)) - 1u;
                         constexpr int kStride = COPIES * 4;  // bytes between table entries
                         constexpr int kLog = COPIES == 32 ? 7 : 2;
@@ -872,22 +948,26 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
                         for (int pp = 0; pp < 16; ++pp) {
                             const int tt = POS0 + 2 * pp;
                             const int sh = F::kBits * (tt % F::kCW);
-                            const uint32_t w = W[tt / F::kCW];
+                            const uint32_t w = WW[O + tt / F::kCW];
                             const uint32_t off =
                                 (sh >= kLog ? (w >> (sh - kLog)) : (w << (kLog - sh))) & (kMask * kStride);
                             out[pp] = hmul2_bits<XT>(lds32(lutl + off), pp < 8 ? rr0 : rr1);
                         }
                     };
+                    using I0 = std::integral_constant<int, 0>;
                     if constexpr (LEVELS == 8) {
-                        switch (pos0) {
-                            case 0: dec(std::integral_constant<int, 0>{}); break;
-                            case 2: dec(std::integral_constant<int, 2>{}); break;
-                            case 4: dec(std::integral_constant<int, 4>{}); break;
-                            case 6: dec(std::integral_constant<int, 6>{}); break;
-                            default: dec(std::integral_constant<int, 8>{}); break;
+                        switch (pos0) {  // pos0 fixes o: (0,0) (2,3) (4,2) (6,1) (8,0)
+                            case 0: dec(I0{}, I0{}); break;
+                            case 2: dec(std::integral_constant<int, 2>{}, std::integral_constant<int, 3>{}); break;
+                            case 4: dec(std::integral_constant<int, 4>{}, std::integral_constant<int, 2>{}); break;
+                            case 6: dec(std::integral_constant<int, 6>{}, std::integral_constant<int, 1>{}); break;
+                            default: dec(std::integral_constant<int, 8>{}, I0{}); break;
                         }
+                    } else if constexpr (LEVELS == 4) {
+                        if (o == 0) dec(I0{}, I0{});
+                        else dec(I0{}, std::integral_constant<int, 2>{});
                     } else {
-                        dec(std::integral_constant<int, 0>{});
+                        dec(I0{}, I0{});
                     }
                     const uint32_t arow = arow0 + s * kABytes;
 #pragma unroll
@@ -895,7 +975,7 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
                         sts128(arow ^ ((4 * h + c4) << 4), out[4 * c4], out[4 * c4 + 1], out[4 * c4 + 2],
                                out[4 * c4 + 3]);
                     fence_async_smem();
-                    mbar_arrive(fullA + s);
+                    mbar_arrive(full + s);
                 }
                 if (++sub == SPC || kc == nk - 1) {
                     mbar_arrive(cempty + cc % kChunkSlots);
@@ -903,27 +983,44 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
                     sub = 0;
                 }
             }
-            if (!ok) break;
-            mbar_arrive(sempty);  // scale block no longer read (row scales kept in rowscale)
-            if (!mbar_wait(tile_full, tile_it & 1, abort_flag)) { ok = false; break; }
+        }
+    } else {
+        // ------------------------------------------------ epilogue: accumulator -> y rows of the sorted pairs
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int m = quarter * 32 + lane;
+        uint32_t tile_it = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x, ++tile_it) {
+            int e, mt, nt, i0, nvalid;
+            item_coords(item, e, mt, nt, i0, nvalid);
+            const int buf = tile_it & 1;
+            if (!mbar_wait(tile_full + buf, (tile_it >> 1) & 1, abort_flag)) break;
             tc_fence_after();
-            if (!dec_sync()) { ok = false; break; }
-            const int m = quarter * 32 + lane;
-            const float rs = rowscale[m];
-            for (int c0 = part * 64; c0 < part * 64 + 64; c0 += 32) {
-                if (c0 < nvalid) {
-                    uint32_t v[32];
-                    tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+            const int64_t ybase = (int64_t)i0 * p.rows + mt * kBM + m;
+            const bool ksplit = ((nvalid + 15) & ~15) <= 128 && nk >= 2;  // as the MMA threads decided
+            const uint32_t t0 = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kNT);
+            if (ksplit) {
+                for (int c0 = 0; c0 < nvalid; c0 += 16) {  // the two K halves' partial sums
+                    uint32_t v[16], w[16];
+                    tc_ld16(t0 + (uint32_t)c0, v);
+                    tc_ld16(t0 + 128u + (uint32_t)c0, w);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < 16; ++j)
                         if (c0 + j < nvalid)
-                            store_from_float(p.y, (int64_t)(i0 + c0 + j) * p.rows + m0 + m, p.ydt,
-                                             __uint_as_float(v[j]) * rs);
-                    }
+                            store_from_float(p.y, ybase + (int64_t)(c0 + j) * p.rows, p.ydt,
+                                             __uint_as_float(v[j]) + __uint_as_float(w[j]));
+                }
+            } else {
+                for (int c0 = 0; c0 < nvalid; c0 += 32) {
+                    uint32_t v[32];
+                    tc_ld32(t0 + (uint32_t)c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < nvalid)
+                            store_from_float(p.y, ybase + (int64_t)(c0 + j) * p.rows, p.ydt, __uint_as_float(v[j]));
                 }
             }
             tc_fence_before();
-            mbar_arrive(tile_empty);
+            mbar_arrive(tile_empty + buf);
         }
     }
 
@@ -931,15 +1028,45 @@ __global__ void __launch_bounds__(kThreads2, 1) gather_qmm2_kernel(const QmmPara
     if (tid == 0 && *abort_flag && p.err) atomicOr(p.err, TQ_DEVERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kNT) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kNT) : "memory");
     }
 }
 
-size_t qmm2_smem_bytes(int levels, int experts) {
-    const int copies = levels == 16 ? 1 : 32;
-    return 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes + (size_t)kChunkSlots * kChunkBytes +
-           kScaleBlock + (size_t)levels * levels * copies * 4 + 5 * kBM * 4 + 32 * 8 + 32 +
-           (size_t)(experts + 1) * 4;
+// Token rows into sorted pair order: xs[i] = x[perm[i] / k] (zero and BAD_ID for
+// an out-of-range perm entry).  One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+                                                          int P, int k, int vecs, uint4* __restrict__ xs,
+                                                          uint32_t* err) {
+    const int wpb = blockDim.x >> 5, lane = threadIdx.x & 31;
+    for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < P; i += gridDim.x * wpb) {
+        const int f = __ldg(perm + i);
+        const bool ok = f >= 0 && f < P;
+        if (!ok && lane == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
+        const uint4* src = x + (size_t)(ok ? f / k : 0) * vecs;
+        uint4* dst = xs + (size_t)i * vecs;
+#pragma unroll 4
+        for (int v = lane; v < vecs; v += 32) dst[v] = ok ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <int LEVELS, int G>
+size_t qmm2_smem_bytes(int experts) {
+    return (size_t)Q2Fmt<LEVELS, G>::kSmem + (size_t)(experts + 1) * 8;
+}
+
+template <int LEVELS>
+size_t qmm2_smem_bytes_g(int G, int experts) {
+    switch (G) {
+        case 16: return qmm2_smem_bytes<LEVELS, 16>(experts);
+        case 32: return qmm2_smem_bytes<LEVELS, 32>(experts);
+        case 64: return qmm2_smem_bytes<LEVELS, 64>(experts);
+        default: return qmm2_smem_bytes<LEVELS, 128>(experts);
+    }
+}
+
+size_t qmm2_smem_for(int levels, int G, int experts) {
+    return levels == 4 ? qmm2_smem_bytes_g<4>(G, experts)
+                       : levels == 8 ? qmm2_smem_bytes_g<8>(G, experts) : qmm2_smem_bytes_g<16>(G, experts);
 }
 
 size_t qmm_smem_bytes(int levels, int experts) {
@@ -959,55 +1086,101 @@ tq_status launch_qmm(const QmmParams& p, cudaStream_t st) {
     return launch_status();
 }
 
-// The staged kernel holds a tile's scale block in 128 bytes per row: it takes
-// an even group count of at most 64 per row; other shapes use the first kernel.
-bool staged_fits(const QmmParams& p, int G, int levels) {
-    const int ngroups = p.cols / G;
-    return ngroups <= 64 && ngroups % 2 == 0 && p.ess % 2 == 0 && aligned(p.scales, 4) &&
-           qmm2_smem_bytes(levels, p.experts) <= 227 * 1024;
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link
+// against the driver library).
+EncodeFn tensor_map_encoder() {
+    static const EncodeFn fn = []() -> EncodeFn {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeFn>(f);
+    }();
+    return fn;
 }
 
-template <int LEVELS, int G, int XT>
-tq_status launch_qmm2(const QmmParams& p, cudaStream_t st) {
-    const size_t smem = qmm2_smem_bytes(LEVELS, p.experts);
-    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, XT>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+// The staged kernel holds a tile's scale block in 128 bytes per row (an even
+// group count of at most 64) and reads codes by tensor copies (rows and experts
+// a multiple of 16 bytes apart); other shapes use the first kernel.
+bool staged_fits(const QmmParams& p, int G, int levels) {
+    const int ngroups = p.cols / G;
+    return ngroups <= 64 && ngroups % 2 == 0 && p.ess % 2 == 0 && aligned(p.scales, 4) && aligned(p.codes, 16) &&
+           p.row_stride % 4 == 0 && p.esw % 4 == 0 && p.row_stride <= (int64_t)1 << 31 &&
+           qmm2_smem_for(levels, G, p.experts) <= (size_t)kSmemLimit && tensor_map_encoder() != nullptr;
+}
+
+// Tensor maps of the pair rows (P x cols, 2-byte elements) and of the codes.
+bool encode_maps(const QmmParams& p, const void* rows_base, QmmMaps& m) {
+    const EncodeFn enc = tensor_map_encoder();
+    for (int i = 0; i < 5; ++i) {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.cols, (cuuint64_t)p.P};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.cols * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows[i]};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&m.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(rows_base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    const int64_t esw = p.experts > 1 ? p.esw : (int64_t)p.rows * p.row_stride;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.row_stride, (cuuint64_t)p.rows, (cuuint64_t)p.experts};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.row_stride * 4, (cuuint64_t)esw * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)kBM, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(&m.c, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(p.codes), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    gather_qmm2_kernel<LEVELS, G, XT><<<sms > 0 ? sms : 148, kThreads2, smem, st>>>(p);
+    return sms > 0 ? sms : 148;
+}
+
+template <int LEVELS, int G, int XT>
+tq_status launch_qmm2(const QmmParams& p, const QmmMaps& maps, cudaStream_t st) {
+    const size_t smem = qmm2_smem_bytes<LEVELS, G>(p.experts);
+    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, XT>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    gather_qmm2_kernel<LEVELS, G, XT><<<sm_count(), kThreads2, smem, st>>>(p, maps);
     return launch_status();
 }
 
 template <int LEVELS, int G, int XT>
-tq_status launch_any(const QmmParams& p, cudaStream_t st) {
-    return staged_fits(p, G, LEVELS) ? launch_qmm2<LEVELS, G, XT>(p, st) : launch_qmm<LEVELS, G, XT>(p, st);
+tq_status launch_any(const QmmParams& p, const QmmMaps* maps, cudaStream_t st) {
+    return maps ? launch_qmm2<LEVELS, G, XT>(p, *maps, st) : launch_qmm<LEVELS, G, XT>(p, st);
 }
 
 template <int LEVELS, int G>
-tq_status dispatch_xt(const QmmParams& p, int xt, cudaStream_t st) {
-    return xt == 0 ? launch_any<LEVELS, G, 0>(p, st) : launch_any<LEVELS, G, 1>(p, st);
+tq_status dispatch_xt(const QmmParams& p, int xt, const QmmMaps* maps, cudaStream_t st) {
+    return xt == 0 ? launch_any<LEVELS, G, 0>(p, maps, st) : launch_any<LEVELS, G, 1>(p, maps, st);
 }
 
 template <int LEVELS>
-tq_status dispatch_g(const QmmParams& p, int group, int xt, cudaStream_t st) {
+tq_status dispatch_g(const QmmParams& p, int group, int xt, const QmmMaps* maps, cudaStream_t st) {
     switch (group) {
-        case 16: return dispatch_xt<LEVELS, 16>(p, xt, st);
-        case 32: return dispatch_xt<LEVELS, 32>(p, xt, st);
-        case 64: return dispatch_xt<LEVELS, 64>(p, xt, st);
-        case 128: return dispatch_xt<LEVELS, 128>(p, xt, st);
+        case 16: return dispatch_xt<LEVELS, 16>(p, xt, maps, st);
+        case 32: return dispatch_xt<LEVELS, 32>(p, xt, maps, st);
+        case 64: return dispatch_xt<LEVELS, 64>(p, xt, maps, st);
+        case 128: return dispatch_xt<LEVELS, 128>(p, xt, maps, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
 
 }  // namespace
 
-extern "C" size_t tq_gather_qmm_workspace_bytes(int32_t experts) { return 0; }
+extern "C" size_t tq_gather_qmm_workspace_bytes(int32_t P, int32_t cols, int32_t per_pair_input) {
+    return per_pair_input || P <= 0 || cols <= 0 ? 0 : (size_t)P * (size_t)cols * 2;
+}
 
 extern "C" tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtype xdt, const int32_t* perm,
                                    const int32_t* offsets, int32_t P, int32_t k, int32_t per_pair_input, void* y,
                                    tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream) {
-    (void)ws;
-    (void)ws_bytes;
     if (!w || !w->codes || !w->scales || !w->cb.centroids) return TQ_ERR_INVALID;
     if (w->experts <= 0 || w->experts > kMaxExperts || w->rows <= 0 || w->cols <= 0) return TQ_ERR_INVALID;
     if (!(w->group == 16 || w->group == 32 || w->group == 64 || w->group == 128) || w->cols % w->group)
@@ -1022,6 +1195,8 @@ extern "C" tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtyp
     if (w->rows % kBM || w->cols % kBK) return TQ_ERR_UNSUPPORTED;
     if (!offsets || (P > 0 && (!x || !y || (!per_pair_input && !perm)))) return TQ_ERR_INVALID;
     if (!aligned(x, 16)) return TQ_ERR_INVALID;
+    const size_t need = tq_gather_qmm_workspace_bytes(P, w->cols, per_pair_input);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return TQ_ERR_INVALID;
     if (P == 0) return TQ_OK;
     QmmParams p{};
     p.codes = w->codes;
@@ -1044,10 +1219,25 @@ extern "C" tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtyp
     p.err = err;
     const int xt = xdt == TQ_F16 ? 0 : 1;
     cudaStream_t st = as_stream(stream);
+    QmmMaps maps;
+    const QmmMaps* mp = nullptr;
+    if (staged_fits(p, w->group, w->cb.levels)) {
+        const void* rows = x;
+        if (!per_pair_input) {  // token rows into sorted pair order first
+            const int vecs = w->cols / 8;
+            gather_rows_kernel<<<sm_count() * 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), perm, P, k, vecs,
+                                                               reinterpret_cast<uint4*>(ws), err);
+            const tq_status s = launch_status();
+            if (s != TQ_OK) return s;
+            rows = ws;
+        }
+        if (!encode_maps(p, rows, maps)) return TQ_ERR_CUDA;
+        mp = &maps;
+    }
     switch (w->cb.levels) {
-        case 4: return dispatch_g<4>(p, w->group, xt, st);
-        case 8: return dispatch_g<8>(p, w->group, xt, st);
-        case 16: return dispatch_g<16>(p, w->group, xt, st);
+        case 4: return dispatch_g<4>(p, w->group, xt, mp, st);
+        case 8: return dispatch_g<8>(p, w->group, xt, mp, st);
+        case 16: return dispatch_g<16>(p, w->group, xt, mp, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
 }

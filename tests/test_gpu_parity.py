@@ -374,7 +374,7 @@ def _qmm_case(lib, levels, group, E, rows, K, T, k, xt, seed):
 
 @pytest.mark.parametrize("levels,group,E,rows,K,T,k", [(8, 64, 12, 256, 1024, 300, 8), (16, 64, 6, 128, 512, 70, 2),
                                                        (4, 32, 5, 128, 640, 40, 3), (8, 128, 3, 384, 1536, 9, 2),
-                                                       (16, 16, 4, 128, 512, 50, 2),
+                                                       (16, 16, 4, 128, 512, 50, 2), (8, 16, 3, 128, 64, 20, 2),
                                                        # more than 64 or an odd number of groups per row
                                                        (8, 16, 3, 128, 1280, 40, 2), (4, 64, 4, 128, 576, 33, 2)])
 def test_gather_qmm_tensor_core(lib, levels, group, E, rows, K, T, k):
