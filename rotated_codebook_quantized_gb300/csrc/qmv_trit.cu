@@ -281,6 +281,11 @@ tq_status launch_trit(const QmvParams& qp, int n_items, cudaStream_t st) {
 // too slow for 128-byte pieces.)
 
 TQ_DEVFN uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+TQ_DEVFN uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
 
 TQ_DEVFN void cp16(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
@@ -292,29 +297,33 @@ TQ_DEVFN void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-constexpr int kPipeNS = 5;  // stages per warp ring
 constexpr int kPipeRPW = 4, kPipeUPW = 8;
+constexpr int kPipeUPL = 4;  // units per lane and stage: lane c takes units c, c + 8, c + 16, c + 24
+constexpr int kPipeNS = 2;   // stages per warp ring (a stage is long enough to hide the load latency)
 
 template <int G>
 struct PipeFmt {
     using F = TritFmt<G>;
-    static constexpr int kCodeBytes = kPipeUPW * F::kUW * 4;       // per row and stage
-    static constexpr int kScaleBytes = kPipeUPW * F::kGPU * 2;     // per row and stage (80)
-    static constexpr int kStage = kPipeRPW * (kCodeBytes + kScaleBytes);
+    static constexpr int kS = kPipeUPW * kPipeUPL;               // units per row and stage
+    static constexpr int kCodeRow = kS * F::kUW * 4;              // code bytes per row and stage
+    static constexpr int kScaleRow = kS * F::kGPU * 2;            // scale bytes per row and stage
+    static constexpr int kStage = kPipeRPW * (kCodeRow + kScaleRow);
+    static constexpr int kScaleCopies = (kScaleRow / 16 + kPipeUPW - 1) / kPipeUPW;  // 16-byte copies per lane
+    static_assert(kScaleRow % 16 == 0, "scale row copy");
 };
 
 template <int G>
 __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams tp) {
     using F = TritFmt<G>;
     using B = PipeFmt<G>;
-    constexpr int RPW = kPipeRPW, UPW = kPipeUPW, NS = kPipeNS;
+    constexpr int RPW = kPipeRPW, UPW = kPipeUPW, UPL = kPipeUPL, NS = kPipeNS, S = B::kS;
     constexpr int UW = F::kUW, GPU = F::kGPU, US = F::kUS;
     constexpr int nwarps = 8;
     const QmvParams& p = tp.q;
     extern __shared__ __align__(16) uint32_t sm[];
     uint32_t* lut = sm;                                           // [81][32]
-    uint32_t* xb = lut + 81 * 32;                                 // [nsteps*8 units][US]
-    const int nunits_pad = tp.nsteps * UPW;
+    uint32_t* xb = lut + 81 * 32;                                 // [nsteps * S units][US]
+    const int nunits_pad = tp.nsteps * S;
     uint8_t* ring0 = reinterpret_cast<uint8_t*>(xb + nunits_pad * US);  // [8 warps][NS][stage]
     float* rowsum = reinterpret_cast<float*>(ring0 + nwarps * NS * B::kStage);  // [max tasks per CTA][RPW]
 
@@ -331,10 +340,12 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
     const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
     const int t_end = (int)((int64_t)(blockIdx.x + 1) * tp.total_tasks / gridDim.x);
     const int r = lane / UPW, c = lane % UPW;
-    const uint32_t* lut_lane = lut + lane;
+    // shared address of table entry v of this lane is lut_bias + ((0x4B400000 + v) << 7), mod 2^32
+    const uint32_t lut_bias = smem_addr(lut + lane) - (0x4B400000u << 7);
     const int ngroups = p.ngroups;
-    const int nst = tp.nsteps;  // stages (of 8 units) per task
+    const int nst = tp.nsteps;  // stages (of S units) per task
     const int tpi = tp.tasks_per_item;
+    const int64_t row_stride = p.row_stride;
     uint8_t* ring = ring0 + warp * NS * B::kStage;
     int cur_vec = -1;
 
@@ -367,35 +378,49 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
         const int f_end = (int)((int64_t)(warp + 1) * nunits_seg / nwarps);
         const int L = f_end - f_begin;
 
-        // producer position (task, stage) and its row pointers
+        // Producer: task pt, stage ps; pcode/pscale point at this lane's first unit of the stage.
         int pt = s0 + f_begin / nst, ps = f_begin % nst, pslot = 0;
         const uint32_t* pcode = nullptr;
         const uint16_t* pscale = nullptr;
+        int pword = 0;  // word index of this lane's first unit in the row
+        int pgrp = 0;   // first scale group of this lane's first scale chunk
+        const int rs32 = (int)row_stride;
         auto set_prod_task = [&]() {
             int e, v;
             item_info(pt / tpi, e, v);
-            if (e < 0 || e >= p.experts) e = 0;  // rows of a bad id are written as zero below
+            if (e < 0 || e >= p.experts) e = 0;  // rows of a bad id are summed as zero below
             const int row = min((pt % tpi) * RPW + r, p.rows - 1);
-            pcode = p.codes + (int64_t)e * p.expert_stride_w + (int64_t)row * p.row_stride;
+            pcode = p.codes + (int64_t)e * p.expert_stride_w + (int64_t)row * row_stride;
             pscale = p.scales + (int64_t)e * p.expert_stride_s + (int64_t)row * ngroups;
+            pword = (ps * S + c) * UW;
+            pgrp = ps * S * GPU + c * 8;
         };
         if (L > 0) set_prod_task();
         auto issue = [&]() {
             uint8_t* dst = ring + pslot * B::kStage;
-            const int64_t w0 = (int64_t)(ps * UPW + c) * UW;  // this lane's unit
 #pragma unroll
-            for (int m = 0; m < UW; m += 4) {
-                const int64_t wi = w0 + m;
-                const bool in = wi < p.row_stride;
-                cp16(dst + r * B::kCodeBytes + (c * UW + m) * 4, pcode + (in ? wi : 0), in ? 16u : 0u);
+            for (int j = 0; j < UPL; ++j) {
+#pragma unroll
+                for (int m = 0; m < UW; m += 4) {
+                    const int wi = pword + j * UPW * UW + m;
+                    const bool in = wi < rs32;  // past the padded row: zero
+                    cp16(dst + r * B::kCodeRow + ((c + j * UPW) * UW + m) * 4, pcode + (in ? wi : 0), in ? 16u : 0u);
+                }
             }
-            if (c < B::kScaleBytes / 16) {  // 5 lanes per row copy its 80 bytes of scales
-                const int64_t g0 = (int64_t)ps * UPW * GPU + c * 8;
-                const bool in = g0 < ngroups;  // scale rows are whole 16-byte chunks
-                cp16(dst + RPW * B::kCodeBytes + r * B::kScaleBytes + c * 16, pscale + (in ? g0 : 0), in ? 16u : 0u);
+#pragma unroll
+            for (int q = 0; q < B::kScaleCopies; ++q) {  // the row's scale bytes, 16 per lane and copy
+                const int chunk = c + q * UPW;
+                if (chunk * 16 < B::kScaleRow) {
+                    const int g0 = pgrp + q * UPW * 8;
+                    const bool in = g0 < ngroups;  // scale rows are whole 16-byte chunks
+                    cp16(dst + RPW * B::kCodeRow + r * B::kScaleRow + chunk * 16, pscale + (in ? g0 : 0),
+                         in ? 16u : 0u);
+                }
             }
             cp_commit();
             pslot = pslot + 1 == NS ? 0 : pslot + 1;
+            pword += S * UW;
+            pgrp += S * GPU;
             if (++ps == nst) {
                 ps = 0;
                 ++pt;
@@ -469,16 +494,19 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
         }
         float tot = 0.f;
         for (int j = 0; j < L; ++j) {
-            cp_wait<NS - 2>();
-            __syncwarp();
-            const int u = cs * UPW + c;
+            cp_wait<NS - 2>();  // stage j has landed
+            __syncwarp();       // and every lane is done with the slot of stage j - 1
+            if (j + NS - 1 < L) issue(); else cp_commit();  // stage j + NS - 1 into that slot
             const uint8_t* stg = ring + cslot * B::kStage;
-            if (u < tp.units && !cbad) {
+            // Units past the row's last one read zero words and zero input blocks.
+#pragma unroll
+            for (int ju = 0; ju < UPL; ++ju) {
+                const int uloc = c + ju * UPW;
+                const uint32_t* blk = xb + (cs * S + uloc) * US;
+                const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(stg + r * B::kCodeRow + uloc * UW * 4);
                 uint32_t acc[GPU];
 #pragma unroll
                 for (int g = 0; g < GPU; ++g) acc[g] = 0u;
-                const uint32_t* blk = xb + u * US;
-                const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(stg + r * B::kCodeBytes + c * UW * 4);
 #pragma unroll
                 for (int w4 = 0; w4 < UW; w4 += 4) {
                     const uint4 wq = *reinterpret_cast<const uint4*>(wsrc + w4);
@@ -493,38 +521,54 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
                         const uint32_t word = wv[wi];
                         const uint32_t hh = word / 59049u;
                         const uint32_t ll = word - hh * 59049u;
+                        // Digits of each half h < 3^10 in fp32, every value an integer below 2^24.
+                        // With M = 1.5 * 2^23 (unit spacing), adding M rounds to an integer, and
+                        // round((h - 364) / 729) = floor(h / 729) for every h (the remainder offset
+                        // stays within 0.4993 of zero); the same with 4 and 9 for the remainder.
+                        // t1, t2 hold M + the table index of digits 9..6 and 5..2 of a half, t3 the
+                        // index 9 (h0 % 9) + (h1 % 9) of both halves' last two digits; their bits
+                        // (0x4B400000 + v) << 7 address the per-lane table of 128-byte-spaced entries.
+                        float t1[2], t2[2], b2[2];
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            uint32_t Fx = (half == 0 ? hh : ll) * 72736u + 8860u;
-                            const int pb = half * 5;
-                            const uint32_t v1 = __umulhi(Fx, 81u);
-                            Fx *= 81u;
-                            const uint32_t v2 = __umulhi(Fx, 81u);
-                            Fx *= 81u;
-                            const uint32_t v3 = __umulhi(Fx, 9u);
-                            const uint32_t e1 = lut_lane[v1 << 5], e2 = lut_lane[v2 << 5], e3 = lut_lane[v3 << 5];
+                            const float hb = __uint_as_float((half == 0 ? hh : ll) | 0x4B000000u) - 8388972.0f;
+                            t1[half] = fmaf(hb, 1.0f / 729.0f, 12582912.0f);              // M + h / 729
+                            const float b1 = fmaf(t1[half] - 12582912.0f, -729.0f, hb);   // h % 729 - 364
+                            t2[half] = fmaf(b1, 1.0f / 9.0f, 12582952.0f);                // M + h % 729 / 9
+                            b2[half] = fmaf(t2[half] - 12582912.0f, -9.0f, b1);           // h % 9 - 364
+                        }
+                        const float t3 = fmaf(b2[0], 9.0f, b2[1] + 12586552.0f);  // M + 9 (h0 % 9) + h1 % 9
+                        const uint32_t e3 = lds_u32(lut_bias + (__float_as_uint(t3) << 7));
 #define TQ_GRP(pp) ((20 * w + 18 - 2 * (pp)) / G)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int pb = half * 5;
+                            const uint32_t e1 = lds_u32(lut_bias + (__float_as_uint(t1[half]) << 7));
+                            const uint32_t e2 = lds_u32(lut_bias + (__float_as_uint(t2[half]) << 7));
                             acc[TQ_GRP(pb + 0)] = dp2a_lo(xp[pb + 0], e1, acc[TQ_GRP(pb + 0)]);
                             acc[TQ_GRP(pb + 1)] = dp2a_hi(xp[pb + 1], e1, acc[TQ_GRP(pb + 1)]);
                             acc[TQ_GRP(pb + 2)] = dp2a_lo(xp[pb + 2], e2, acc[TQ_GRP(pb + 2)]);
                             acc[TQ_GRP(pb + 3)] = dp2a_hi(xp[pb + 3], e2, acc[TQ_GRP(pb + 3)]);
-                            acc[TQ_GRP(pb + 4)] = dp2a_hi(xp[pb + 4], e3, acc[TQ_GRP(pb + 4)]);
-#undef TQ_GRP
                         }
+                        acc[TQ_GRP(4)] = dp2a_lo(xp[4], e3, acc[TQ_GRP(4)]);  // half 0's last digits: bytes 0, 1
+                        acc[TQ_GRP(9)] = dp2a_hi(xp[9], e3, acc[TQ_GRP(9)]);  // half 1's: bytes 2, 3
+#undef TQ_GRP
                     }
                 }
                 const uint16_t* ssrc =
-                    reinterpret_cast<const uint16_t*>(stg + RPW * B::kCodeBytes + r * B::kScaleBytes) + c * GPU;
+                    reinterpret_cast<const uint16_t*>(stg + RPW * B::kCodeRow + r * B::kScaleRow) + uloc * GPU;
                 const float* abu = reinterpret_cast<const float*>(blk + F::kAB);
+                // Groups past the last column have a_g = b_g = 0 and zero-filled scales.  The
+                // group sum |acc| <= 2 G 32767 < 2^22 becomes a float exactly by adding it to 1.5 * 2^23.
 #pragma unroll
                 for (int g = 0; g < GPU; ++g) {
-                    const float sv = (u * GPU + g < ngroups) ? half_bits_to_float(ssrc[g]) : 0.f;
-                    tot = fmaf(sv, fmaf(abu[2 * g], (float)(int)acc[g], abu[2 * g + 1]), tot);
+                    const float accf = __int_as_float((int)acc[g] + 0x4B400000) - 12582912.0f;
+                    tot = fmaf(half_bits_to_float(ssrc[g]), fmaf(abu[2 * g], accf, abu[2 * g + 1]), tot);
                 }
             }
             cslot = cslot + 1 == NS ? 0 : cslot + 1;
             if (++cs == nst || j == L - 1) {  // task finished or this warp's share ends: add the row sums
-                float v = tot;
+                float v = cbad ? 0.f : tot;
 #pragma unroll
                 for (int m = 1; m < UPW; m <<= 1) v += __shfl_xor_sync(kFull, v, m);
                 if (c == 0) atomicAdd(rowsum + (ct - s0) * RPW + r, v);
@@ -540,8 +584,6 @@ __global__ void __launch_bounds__(256, 3) qmv_trit_pipe_kernel(const TritParams 
                     }
                 }
             }
-            __syncwarp();
-            if (j + NS - 1 < L) issue(); else cp_commit();
         }
         cp_wait<0>();
         __syncthreads();  // all row sums of the segment complete
@@ -560,7 +602,7 @@ tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
     TritParams tp{};
     tp.q = qp;
     tp.units = (qp.cols + F::kUT - 1) / F::kUT;
-    tp.nsteps = (tp.units + kPipeUPW - 1) / kPipeUPW;
+    tp.nsteps = (tp.units + B::kS - 1) / B::kS;
     tp.tasks_per_item = (qp.rows + kPipeRPW - 1) / kPipeRPW;
     tp.n_items = n_items;
     const int64_t total = (int64_t)n_items * tp.tasks_per_item;
@@ -573,27 +615,33 @@ tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    const size_t smem_fixed = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * kPipeUPW * F::kUS) +
+    const size_t smem_fixed = 4 * ((size_t)81 * 32 + (size_t)tp.nsteps * B::kS * F::kUS) +
                               (size_t)8 * kPipeNS * B::kStage;
     const void* kfn = (const void*)qmv_trit_pipe_kernel<G>;
-    int per_sm = 0;
-    // occupancy with a row-sum buffer of up to 256 tasks (the limit must be raised first)
-    if (smem_fixed + 4096 > 200 * 1024) return TQ_ERR_UNSUPPORTED;
-    if (ensure_smem(kfn, smem_fixed + 4096) != cudaSuccess) return TQ_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_trit_pipe_kernel<G>, 256,
-                                                      smem_fixed + 4096) != cudaSuccess || per_sm <= 0)
-        per_sm = 1;
-    // one wave of resident CTAs, but at most 128 tasks per CTA (bounds the row-sum buffer)
-    int64_t grid = (int64_t)sms * per_sm;
-    const int64_t max_grid = (total + 7) / 8;
-    if (grid > max_grid) grid = max_grid;
-    if (grid < (total + 127) / 128) grid = (total + 127) / 128;
-    if (grid < 1) grid = 1;
-    if (grid > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
-    max_grid_tasks = (int)((total + grid - 1) / grid) + 1;
-    const size_t smem = smem_fixed + (size_t)max_grid_tasks * kPipeRPW * 4;
-    if (smem > 200 * 1024) return TQ_ERR_UNSUPPORTED;
-    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    // The most resident CTAs per SM (3, 2 or 1) whose shared memory, including the row-sum
+    // buffer of the tasks each then takes, fits; one wave of them, at most 128 tasks per CTA.
+    int64_t grid = 0;
+    size_t smem = 0;
+    for (int per_sm = 3; per_sm >= 1 && grid == 0; --per_sm) {
+        int64_t g = (int64_t)sms * per_sm;
+        const int64_t max_grid = (total + 7) / 8;
+        if (g > max_grid) g = max_grid;
+        if (g < (total + 127) / 128) g = (total + 127) / 128;
+        if (g < 1) g = 1;
+        if (g > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+        max_grid_tasks = (int)((total + g - 1) / g) + 1;
+        const size_t need = smem_fixed + (size_t)max_grid_tasks * kPipeRPW * 4;
+        if (need > 200 * 1024) continue;
+        if (ensure_smem(kfn, need) != cudaSuccess) return TQ_ERR_CUDA;
+        int fit = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qmv_trit_pipe_kernel<G>, 256, need) != cudaSuccess)
+            return TQ_ERR_CUDA;
+        if (fit >= per_sm || per_sm == 1) {
+            grid = g;
+            smem = need;
+        }
+    }
+    if (grid == 0) return TQ_ERR_UNSUPPORTED;
     qmv_trit_pipe_kernel<G><<<(unsigned)grid, 256, smem, st>>>(tp);
     return launch_status();
 }
@@ -605,7 +653,7 @@ tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
 tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t st) {
     // Staged pipeline when every copy is 16-byte aligned: 16-byte code rows
     // (always), scale rows and expert scale strides in whole 16-byte chunks.
-    const bool pipe_ok = (group == 16 || group == 32) && ((int64_t)p.ngroups * 2) % 16 == 0 &&
+    const bool pipe_ok = (group == 16 || group == 32) && ((int64_t)p.ngroups * 2) % 16 == 0 && p.row_stride < (1 << 30) &&
                          (p.expert_stride_s * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 &&
                          (reinterpret_cast<uintptr_t>(p.codes) & 15) == 0;
     if (pipe_ok) return group == 16 ? launch_trit_pipe<16>(p, n_items, st) : launch_trit_pipe<32>(p, n_items, st);
