@@ -246,6 +246,92 @@ def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
                        "min_pairs_per_expert": int(counts.min())}}
 
 
+def graph_time_us(torch, fn, flush, iters=20, skip=3):
+    """Median device time (us) of one CUDA-graph replay of fn(), L2 flushed before each replay."""
+    dev = flush.device
+    fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            fn()
+    torch.cuda.current_stream().wait_stream(st)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        g.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    t = sorted(ev[i][0].elapsed_time(ev[i][1]) for i in range(skip, iters))
+    return t[len(t) // 2] * 1e3
+
+
+def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
+    """The other hot-path calls at the pages' workload shapes, each timed alone (HBM-bound: GB/s and
+    fraction of the measured copy peak).  Algorithmic bytes: unpadded code words + fp16 scales of
+    the matrices a call reads (per pair for multi_gather), KV codes + scales for attention, inputs
+    read + codes and scales written for the encoders."""
+    hbm = peaks["hbm_gbs"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
+    out = {}
+
+    def rec(name, us, nbytes, **kw):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = dict(us=us, bytes=nbytes, gbs=gbs, frac_of_hbm_peak=gbs / hbm, **kw)
+
+    # dense 3-bit qmv, 11008 x 4096, group 128, T in {1, 4, 16}
+    N, K, G = 11008, 4096, 128
+    qd = random_bit_bank(torch, tq, dev, gen, 1, N, K, 8, G)
+    wbytes = N * (tq.row_words(8, K) * 4 + (K // G) * 2)
+    for T in (1, 4, 16):
+        x = torch.randn((T, K), generator=gen, device=dev)
+        rec(f"dense_qmv_3bit_T{T}", graph_time_us(torch, lambda: tq.qmv(qd, x), flush), wbytes,
+            shape="11008 x 4096, 3-bit, group 128")
+    # encode (rotate, group RMS, snap, pack) of the same matrix from bf16
+    Wb = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    rot = tq.Rotation(K, 4096, seed=11, device=dev)
+    cb8 = tq.Codebook(8, device=dev)
+    rec("quantize_3bit_11008x4096", graph_time_us(torch, lambda: tq.quantize(Wb, G, rot, cb8), flush),
+        N * K * 2 + wbytes, shape="bf16 in, 3-bit codes + fp16 scales out")
+    del Wb
+    # decode down projection alone: multi_gather_qmv over the 8 routed ternary experts
+    ids = torch.tensor([(5 + 41 * j) % qdn.experts for j in range(TOPK)], dtype=torch.int32, device=dev)
+    h = torch.randn((TOPK, INTER), generator=gen, device=dev)
+    _, dn_b = packed_bytes_per_expert()
+    rec("decode_down_multi_gather_ternary", graph_time_us(torch, lambda: tq.multi_gather_qmv(qdn, h, ids), flush),
+        TOPK * dn_b, shape="8 experts x 7168 x 2048, ternary group 16")
+    # per-pair inputs at T = 8 (prefill-shaped down projection): 64 pairs over 128 experts, 3-bit group 64
+    qp = random_bit_bank(torch, tq, dev, gen, P_E, P_H, P_I, 8, P_G)
+    logits = torch.from_numpy(wl.router_logits(P_SEED, 8, P_E, zipf=1.1)).to(dev)
+    pids, _, _, _, _ = tq.moe_route(logits, P_K, sort=False)
+    hp = torch.randn((8 * P_K, P_I), generator=gen, device=dev)
+    per_exp = P_H * (tq.row_words(8, P_I) * 4 + (P_I // P_G) * 2)
+    rec("multi_gather_3bit_T8", graph_time_us(torch, lambda: tq.multi_gather_qmv(qp, hp, pids.view(-1)), flush),
+        8 * P_K * per_exp, shape="64 pairs (8 tokens x top-8 of 128) x 4096 x 1536, 3-bit group 64",
+        distinct_experts=int(torch.unique(pids).numel()))
+    del qp
+    # KV cache: compress 131072 tokens x 8 heads x 128 (8-bit K, 3-bit V, group 32), then one decode read
+    ctx, Hkv, D, KG = 131072, 8, 128, 32
+    kvc = tq.KVCache(ctx, Hkv, D, KG, tq.Codebook(256, device=dev), tq.Codebook(8, device=dev),
+                     tq.Rotation(D, D, seed=13, device=dev), device=dev)
+    kk = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    vv = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    kv_bytes = Hkv * ctx * ((kvc.kw + kvc.vw) * 4 + 2 * (D // KG) * 2)
+    rec("kv_quantize_131072", graph_time_us(torch, lambda: tq.kv_quantize(kvc, kk, vv, pos=0), flush, iters=8),
+        2 * ctx * Hkv * D * 2 + kv_bytes, shape="131072 tokens x 8 kv heads x 128, K 8-bit / V 3-bit, group 32")
+    del kk, vv
+    kvc.length = ctx
+    q = torch.randn((32, D), generator=gen, device=dev).to(torch.bfloat16)
+    ws = torch.empty(max(int(tq.load().tq_kv_attend_workspace_bytes(32, D, ctx)), 1), dtype=torch.uint8, device=dev)
+    rec("kv_attend_131072", graph_time_us(torch, lambda: tq.kv_attend(kvc, q, ws=ws), flush), kv_bytes,
+        shape="32 query heads (GQA 4:1) over 131072 cached tokens")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -255,6 +341,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--experts", type=int, default=E, help="decode bank size (smaller only for profiling captures)")
     ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill gather-GEMM measurement")
+    ap.add_argument("--skip-extras", action="store_true", help="skip the other calls' measurements")
     ap.add_argument("--_oracle-sample", dest="oracle_sample", type=float, default=None)
     args = ap.parse_args()
 
@@ -324,14 +411,14 @@ def main():
     x_buf = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device=dev)
 
     def step():
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK)
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)  # decode reads experts by id
         xr = tq.rotate(x_buf, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
         hr = tq.swiglu_rotate(gu, INTER, rotI)
         yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    launches_per_step = 8  # route: top-k, scan, compact; rotate; gather; swiglu+rotate; multi-gather; combine
+    launches_per_step = 6  # route top-k; rotate; gather; swiglu+rotate; multi-gather; combine (one kernel each)
 
     # warm up eagerly (first calls set kernel attributes), then capture the step
     logits_buf.copy_(logits_all[0:1])
@@ -404,9 +491,15 @@ def main():
                 "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_ms * 1e3}
     tr = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr):
+        # DRAM bytes per launch from an ncu capture, valid only while the kernel source is unchanged
         d = json.load(open(tr)).get("gather_qmv_gate_up")
         if d:
-            roofline["traffic"] = d
+            import hashlib
+
+            src = open(os.path.join(ROOT, d["kernel_source"]), "rb").read()
+            if hashlib.sha256(src).hexdigest()[:16] == d["kernel_source_sha256_16"]:
+                roofline["traffic"] = d["bytes_per_launch"]
+                roofline["traffic_capture"] = d["capture"]
 
     # end to end through the Python API: pinned host inputs in, result out, every step
     h_logits = torch.from_numpy(wl.router_logits(SEED + 17 * rank + 5, nsteps, nexp)).pin_memory()
@@ -435,6 +528,7 @@ def main():
            "ms_per_step": e2e_ms / args.steps}
 
     prefill = None if args.skip_prefill else measure_prefill(torch, tq, wl, dev, flush, peaks)
+    extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
 
     if rank == 0:
         line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -443,7 +537,7 @@ def main():
                 "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "gather_qmm_tflops": prefill["value"] if prefill else None, "prefill": prefill,
-                "wall_s_timed_loop": wall}
+                "extras": extras, "wall_s_timed_loop": wall}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

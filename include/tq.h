@@ -197,7 +197,10 @@ tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const i
  * offsets[e] = first sorted position of expert e, offsets[E] = T*k.
  * ids, perm, pair_pos: device int32 [T*k]; probs: device f32 [T*k];
  * offsets: device int32 [E+1].  ws: device scratch of at least
- * tq_route_workspace_bytes(E) bytes (contents need not be initialised). */
+ * tq_route_workspace_bytes(E) bytes (contents need not be initialised).
+ * With perm, pair_pos and offsets all NULL only ids and probs are written
+ * (one token's decode reads the experts by id and needs no sorted order);
+ * ws may then be NULL.  pair_pos alone may be NULL when sorting. */
 tq_status tq_moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* probs,
                        int32_t* perm, int32_t* pair_pos, int32_t* offsets, void* ws, size_t ws_bytes,
                        void* stream);

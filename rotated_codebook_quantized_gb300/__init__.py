@@ -277,14 +277,21 @@ def multi_gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
     return y
 
 
-def moe_route(logits, k: int):
-    """-> ids [T,k] int32, probs [T,k] f32, perm [T*k], pair_pos [T*k], offsets [E+1]."""
+def moe_route(logits, k: int, sort: bool = True):
+    """-> ids [T,k] int32, probs [T,k] f32, perm [T*k], pair_pos [T*k], offsets [E+1].
+
+    With sort=False only ids and probs are computed (the other three are None).
+    """
     torch = _torch()
     _contig(logits, "logits")
     T, E = logits.shape
     dev = logits.device
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     probs = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if not sort:
+        _check(load().tq_moe_route(_ptr(logits), T, E, k, _ptr(ids), _ptr(probs), None, None, None, None, 0,
+                                   _stream()), "tq_moe_route")
+        return ids, probs, None, None, None
     perm = torch.empty(T * k, dtype=torch.int32, device=dev)
     pos = torch.empty(T * k, dtype=torch.int32, device=dev)
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)

@@ -14,28 +14,34 @@ namespace {
 
 constexpr int kMaxK = 32;
 
-// One warp per token: k rounds of an arg-max over the not-yet-taken experts
-// (ties to the lower id), then a softmax over the k chosen logits.
+// One warp per token: the row's logits are read once into registers (lane l
+// holds experts l, l + 32, ...), then k rounds of a warp arg-max over the
+// not-yet-taken experts (ties to the lower id), then a softmax over the k
+// chosen logits.  counts (if not NULL) receives each chosen expert's pair count.
+template <int kPer>  // experts per lane: E <= 32 * kPer
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ probs,
                                                          int32_t* __restrict__ counts) {
-    extern __shared__ uint8_t taken_all[];  // [warps][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
-    uint8_t* taken = taken_all + warp * E;
-    for (int i = lane; i < E; i += 32) taken[i] = 0;
-    __syncwarp();
     const float* row = logits + (int64_t)t * E;
-    float chosen_v = 0.f;  // lane j keeps the j-th chosen logit
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = i < E ? __ldg(row + i) : -INFINITY;
+    }
+    unsigned taken = 0;  // bit j: expert lane + 32 j already chosen
+    float chosen_v = 0.f;  // lane r keeps the r-th chosen logit
     for (int r = 0; r < k; ++r) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int i = lane; i < E; i += 32) {
-            if (taken[i]) continue;
-            const float v = row[i];
-            if (v > bv || (v == bv && i < bi) || bi == 0x7fffffff) {
-                bv = v;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {  // ascending ids within the lane: strict > keeps the lower id
+            const int i = lane + 32 * j;
+            if (i < E && !(taken >> j & 1u) && (v[j] > bv || bi == 0x7fffffff)) {
+                bv = v[j];
                 bi = i;
             }
         }
@@ -48,13 +54,12 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                 bi = oi;
             }
         }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == 0) {
-            taken[bi] = 1;
             ids[(int64_t)t * k + r] = bi;
-            atomicAdd(counts + bi, 1);
+            if (counts) atomicAdd(counts + bi, 1);
         }
         if (lane == r) chosen_v = bv;
-        __syncwarp();
     }
     // softmax over the k chosen logits; the first is the largest
     const float mx = __shfl_sync(kFull, chosen_v, 0);
@@ -139,18 +144,23 @@ extern "C" tq_status tq_moe_route(const float* logits, int32_t T, int32_t E, int
                                   void* stream) {
     if (T < 0 || E <= 0 || E > 1024 || k <= 0 || k > kMaxK || k > E) return TQ_ERR_INVALID;
     if ((int64_t)T * k > 0x7fffffffll) return TQ_ERR_INVALID;
-    if (!offsets || !ws || ws_bytes < tq_route_workspace_bytes(E)) return TQ_ERR_INVALID;
-    if (T > 0 && (!logits || !ids || !probs || !perm)) return TQ_ERR_INVALID;
+    const bool sort = perm || pair_pos || offsets;
+    if (sort && (!perm || !offsets || !ws || ws_bytes < tq_route_workspace_bytes(E))) return TQ_ERR_INVALID;
+    if (T > 0 && (!logits || !ids || !probs)) return TQ_ERR_INVALID;
     cudaStream_t st = as_stream(stream);
-    int32_t* counts = reinterpret_cast<int32_t*>(ws);
-    if (cudaMemsetAsync(counts, 0, (size_t)E * 4, st) != cudaSuccess) return TQ_ERR_CUDA;
+    int32_t* counts = sort ? reinterpret_cast<int32_t*>(ws) : nullptr;
+    if (sort && cudaMemsetAsync(counts, 0, (size_t)E * 4, st) != cudaSuccess) return TQ_ERR_CUDA;
     if (T > 0) {
         const int warps = 8;
-        const size_t smem = (size_t)warps * E;
-        route_topk_kernel<<<(T + warps - 1) / warps, warps * 32, smem, st>>>(logits, T, E, k, ids, probs, counts);
+        const dim3 grid((T + warps - 1) / warps), block(warps * 32);
+        if (E <= 128) route_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
+        else if (E <= 256) route_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
+        else if (E <= 512) route_topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
+        else route_topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
         tq_status s = launch_status();
         if (s != TQ_OK) return s;
     }
+    if (!sort) return TQ_OK;
     route_scan_kernel<<<1, 1024, 0, st>>>(counts, E, offsets);
     tq_status s = launch_status();
     if (s != TQ_OK || T == 0) return s;

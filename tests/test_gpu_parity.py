@@ -48,7 +48,8 @@ def test_host_codebook_and_signs_match_oracle(lib):
 
 
 @pytest.mark.parametrize("dim,block,rows,xdt", [(512, 512, 3, "f32"), (7168, 1024, 2, "bf16"), (1536, 512, 5, "bf16"),
-                                                (128, 128, 33, "f32"), (4096, 4096, 1, "bf16"), (2048, 2048, 4, "f32")])
+                                                (128, 128, 33, "f32"), (4096, 4096, 1, "bf16"), (2048, 2048, 4, "f32"),
+                                                (576, 64, 3, "f32"), (1280, 256, 2, "bf16"), (16384, 8192, 1, "f32")])
 def test_rotate(lib, dim, block, rows, xdt):
     x = wl.rng(1, dim).normal(size=(rows, dim)).astype(np.float32)
     if xdt == "bf16":
@@ -227,7 +228,8 @@ def test_dequant_experts(lib):
     np.testing.assert_allclose(outh, ref, rtol=1e-3, atol=1e-7)
 
 
-@pytest.mark.parametrize("T,E,k,zipf", [(1, 384, 8, None), (37, 128, 8, 1.1), (300, 64, 4, None), (5, 16, 16, None)])
+@pytest.mark.parametrize("T,E,k,zipf", [(1, 384, 8, None), (37, 128, 8, 1.1), (300, 64, 4, None), (5, 16, 16, None),
+                                        (3, 1000, 8, None), (9, 200, 6, 1.1)])
 def test_route(lib, T, E, k, zipf):
     logits = wl.router_logits(9, T, E, zipf=zipf)
     if T == 5:
@@ -242,6 +244,11 @@ def test_route(lib, T, E, k, zipf):
     inv = np.empty_like(operm)
     inv[operm] = np.arange(len(operm))
     np.testing.assert_array_equal(pos.cpu().numpy(), inv)
+    # without the sorted order (the one-token decode form): the same ids and weights
+    ids2, probs2, perm2, _, _ = lib.moe_route(_dev(logits), k, sort=False)
+    assert perm2 is None
+    np.testing.assert_array_equal(ids2.cpu().numpy(), oids)
+    np.testing.assert_allclose(probs2.cpu().numpy(), oprobs, rtol=2e-6, atol=1e-7)
 
 
 def test_swiglu_rotate_and_combine(lib):
