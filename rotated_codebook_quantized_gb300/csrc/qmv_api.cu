@@ -100,6 +100,10 @@ extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T
     QmvParams p = make_params(w, x_rot, y, ydt, nullptr);
     p.mode = kModeDense;
     p.T = T;
+    // Bit-packed books at small T take the staged kernel, one vector per item (later vectors
+    // re-read the weights, mostly from L2).  From T = 16 on, the batched kernel below, which
+    // decodes each weight once for up to 4 vectors, is faster (295 vs 268 us at 11008x4096).
+    if (T <= 8 && qmv_bits_ok(p, w->group)) return qmv_bits_run(p, w->group, T, as_stream(stream));
     const int nv = pick_nv(T, host_kpad(w->cb.levels, w->group, w->cols));
     return run(p, w->group, nv, (T + nv - 1) / nv, as_stream(stream));
 }

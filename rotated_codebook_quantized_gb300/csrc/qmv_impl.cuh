@@ -297,6 +297,8 @@ tq_status dispatch_qmv_nv(QmvParams p, int nv, int n_items, cudaStream_t st) {
 
 // Ternary books with one input vector per item (qmv_trit.cu).
 tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
+bool qmv_bits_ok(const QmvParams& p, int group);
+tq_status qmv_bits_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
 
 // One entry point per (levels, group), each compiled in its own translation unit.
 #define TQ_QMV_DECL(L, G) tq_status qmv_run_l##L##_g##G(QmvParams p, int nv, int n_items, cudaStream_t st);
