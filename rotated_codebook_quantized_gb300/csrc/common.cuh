@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 #include <unordered_map>
 
 #include "tq.h"
@@ -16,6 +17,15 @@
 namespace tq {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// fn(integral_constant<int, I>) for I = B .. E-1, expanded at compile time.
+template <int B, int E, class Fn>
+TQ_DEVFN void static_for(Fn&& fn) {
+    if constexpr (B < E) {
+        fn(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(fn);
+    }
+}
 
 // ---------------------------------------------------------------- launch helpers
 

@@ -20,11 +20,11 @@
 // (expert, 128-row tile, 256-pair tile) in expert-major order so that CTAs
 // running together share the expert's codes in L2.  Every wait on an mbarrier
 // is bounded; on expiry the CTA sets TQ_DEVERR_TIMEOUT, drains and frees TMEM.
-#include <cudaTypedefs.h>
 
 #include <type_traits>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 using namespace tq;
 
@@ -41,68 +41,6 @@ constexpr int kDecWarps = 8;             // decoders / epilogue: warps 5..12
 constexpr int kThreads = 32 * (1 + kProdWarps + kDecWarps);
 constexpr int kFirstDec = 1 + kProdWarps;
 constexpr int kMaxExperts = 1024;
-constexpr long long kWaitCycles = 1ll << 31;  // about a second at GB300 clocks
-
-// ---------------------------------------------------------------- PTX wrappers
-
-TQ_DEVFN uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-TQ_DEVFN void mbar_init(uint64_t* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-
-TQ_DEVFN void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-
-// The waiting thread is suspended (issuing nothing) until the phase completes
-// or about kSuspendNs elapse, so idle roles leave the issue slots to the others.
-constexpr uint32_t kSuspendNs = 20000;
-TQ_DEVFN bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait bounded by time only (used to drain in-flight MMAs before freeing TMEM).
-TQ_DEVFN bool mbar_wait_drain(uint64_t* b, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(b, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-// Bounded wait for the phase of parity `parity` to complete.  Returns false
-// (and raises the CTA's abort flag) if it did not within kWaitCycles or if
-// another role already aborted.
-TQ_DEVFN bool mbar_test(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_test(b, parity)) return true;  // common case first: no clock read, no suspension
-    const long long t0 = clock64();
-    while (!mbar_try_wait(b, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-    return true;
-}
-
-TQ_DEVFN void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 TQ_DEVFN void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
@@ -639,24 +577,6 @@ TQ_DEVFN void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
 TQ_DEVFN void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
-TQ_DEVFN void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
-}
-TQ_DEVFN void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-TQ_DEVFN void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
 template <int LEVELS, int G, int XT>
 __global__ void __launch_bounds__(kThreads2, 1)
     gather_qmm2_kernel(const QmmParams p, const __grid_constant__ QmmMaps tm) {
@@ -1084,23 +1004,6 @@ tq_status launch_qmm(const QmmParams& p, cudaStream_t st) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     gather_qmm_kernel<LEVELS, G, XT><<<sms > 0 ? sms : 148, kThreads, smem, st>>>(p);
     return launch_status();
-}
-
-using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link
-// against the driver library).
-EncodeFn tensor_map_encoder() {
-    static const EncodeFn fn = []() -> EncodeFn {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeFn>(f);
-    }();
-    return fn;
 }
 
 // The staged kernel holds a tile's scale block in 128 bytes per row (an even

@@ -66,15 +66,6 @@ struct BitsStage {
     static constexpr int kStage = kRPW * (kCodeRow + kScaleRow);
 };
 
-// fn(integral_constant<int, I>) for I = B .. E-1, expanded at compile time.
-template <int B, int E, class Fn>
-TQ_DEVFN void static_for(Fn&& fn) {
-    if constexpr (B < E) {
-        fn(std::integral_constant<int, B>{});
-        static_for<B + 1, E>(fn);
-    }
-}
-
 TQ_DEVFN uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 TQ_DEVFN void cp16(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr(dst)), "l"(src), "r"(bytes) : "memory");

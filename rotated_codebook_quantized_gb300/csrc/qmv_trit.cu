@@ -26,9 +26,12 @@
 // persistent: each takes a contiguous range of (item, row block) tasks,
 // prepares the quantized input once per distinct input vector, and its warps
 // share the tasks round-robin.
+#include <algorithm>
+#include <cstdlib>
 #include <numeric>
 
 #include "qmv_impl.cuh"
+#include "tma.cuh"
 
 namespace tq {
 namespace {
@@ -646,6 +649,525 @@ tq_status launch_trit_pipe(const QmvParams& qp, int n_items, cudaStream_t st) {
     return launch_status();
 }
 
+// ---------------------------------------------------------------- tensor-copy pipeline (group 16)
+//
+// Warp-specialised version of the staged pipeline, built to cut the
+// instructions per code word and to keep more bytes in flight:
+//  * one producer warp streams the codes and scales with tensor copies (two per
+//    stage: a 16-row x 128-byte code box, 128-byte swizzled, and a 16-row x
+//    80-byte scale box) into per-consumer rings of three slots; rows, words,
+//    groups and expert ids past the tensor read as zeros, so no bounds checks
+//    remain on the data path;
+//  * each consumer lane decodes the same unit of two rows, so one load of the
+//    quantized input serves two code words; a consumer warp covers 16 rows
+//    (rows r and r + 8 for lane row r) and 4 unit columns, and a unit pass that
+//    lies wholly past the row is skipped;
+//  * the table holds signed digits t = d - 1: for an affine three-level book
+//    c[d] = c1 + t * delta,
+//        sum_k c[d_k] x_k = delta * sum_k t_k x_k + c1 * sum_k x_k,
+//    and with one input scale per vector (x = xs * xq, |xq| <= 32767) a group's
+//    integer sum only needs its weight scale: y = delta * xs * sum_g s_g acc_g
+//    (+ c1 * sum_g s_g X_g when the middle level is not zero);
+//  * the dp2a accumulators start at the bits of 1.5 * 2^23, so their final bits
+//    are the float 1.5 * 2^23 + acc exactly (|acc| <= 16 * 32767 < 2^22).
+// Every wait is bounded; on expiry the CTA raises TQ_DEVERR_TIMEOUT, stops, and
+// waits (bounded) for its copies in flight before it exits.
+
+TQ_DEVFN uint32_t dp2a_lo_ss(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+TQ_DEVFN uint32_t dp2a_hi_ss(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+template <int D>
+TQ_DEVFN uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a), "n"(D));
+    return v;
+}
+template <int D>
+TQ_DEVFN uint2 lds_v2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(D));
+    return v;
+}
+template <int D>
+TQ_DEVFN uint32_t lds_w(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(D));
+    return v;
+}
+#ifndef TQ_TC_WARPS
+#define TQ_TC_WARPS 15
+#endif
+// Consumer warps (warp 0 produces): 15 + 1 puts four warps on each scheduler, which
+// leaves each thread up to 128 registers.
+constexpr int kTcWarps = TQ_TC_WARPS;
+constexpr int kTcDepth = 3;                  // slots per consumer warp
+constexpr int kTcSlots = kTcWarps * kTcDepth;
+constexpr int kTcRows = 16;                  // rows per task
+constexpr int kTcS = 8;                      // units per row and stage
+constexpr int kTcCode = kTcRows * kTcS * 16;  // 2048 code bytes per slot: one 128-byte line per row
+constexpr int kTcScale = kTcRows * kTcS * 10;  // 1280 scale bytes per slot: 80 per row
+constexpr int kTcUS = 52;                    // input block words per unit: 4 x 12, = 4 (mod 8)
+constexpr int kTcThreads = 32 * (1 + kTcWarps);
+
+// Barrier `id` over the first `count` threads' warps (count a multiple of 32).
+TQ_DEVFN void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Signal barrier `id` without waiting on it.
+TQ_DEVFN void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+struct TritMaps {
+    CUtensorMap codes;   // [experts][rows][row_stride] words, box 32 x 16 x 1, 128-byte swizzle
+    CUtensorMap scales;  // [experts][rows][ngroups] fp16, box 40 x 16 x 1
+};
+
+// One 20-trit word against its 20 quantized inputs (pair words xp), added into the
+// unit's five group accumulators.  W is the word's index in the unit.
+template <int W>
+TQ_DEVFN void trit_word_signed(uint32_t word, const uint32_t (&xp)[10], uint32_t (&acc)[5], uint32_t lut_bias) {
+    constexpr int G = 16;
+    const uint32_t hh = word / 59049u;
+    const uint32_t ll = word - hh * 59049u;
+    float t1[2], t2[2], b2[2];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const float hb = __uint_as_float((half == 0 ? hh : ll) | 0x4B000000u) - 8388972.0f;
+        t1[half] = fmaf(hb, 1.0f / 729.0f, 12582912.0f);
+        const float b1 = fmaf(t1[half] - 12582912.0f, -729.0f, hb);
+        t2[half] = fmaf(b1, 1.0f / 9.0f, 12582952.0f);
+        b2[half] = fmaf(t2[half] - 12582912.0f, -9.0f, b1);
+    }
+    const float t3 = fmaf(b2[0], 9.0f, b2[1] + 12586552.0f);
+    const uint32_t e3 = lds_u32(lut_bias + (__float_as_uint(t3) << 7));
+    constexpr int g0 = (20 * W + 18) / G, g1 = (20 * W + 16) / G, g2 = (20 * W + 14) / G, g3 = (20 * W + 12) / G,
+                  g4 = (20 * W + 10) / G, g5 = (20 * W + 8) / G, g6 = (20 * W + 6) / G, g7 = (20 * W + 4) / G,
+                  g8 = (20 * W + 2) / G, g9 = (20 * W) / G;
+    {
+        const uint32_t e1 = lds_u32(lut_bias + (__float_as_uint(t1[0]) << 7));
+        const uint32_t e2 = lds_u32(lut_bias + (__float_as_uint(t2[0]) << 7));
+        acc[g0] = dp2a_lo_ss(xp[0], e1, acc[g0]);
+        acc[g1] = dp2a_hi_ss(xp[1], e1, acc[g1]);
+        acc[g2] = dp2a_lo_ss(xp[2], e2, acc[g2]);
+        acc[g3] = dp2a_hi_ss(xp[3], e2, acc[g3]);
+    }
+    {
+        const uint32_t e1 = lds_u32(lut_bias + (__float_as_uint(t1[1]) << 7));
+        const uint32_t e2 = lds_u32(lut_bias + (__float_as_uint(t2[1]) << 7));
+        acc[g5] = dp2a_lo_ss(xp[5], e1, acc[g5]);
+        acc[g6] = dp2a_hi_ss(xp[6], e1, acc[g6]);
+        acc[g7] = dp2a_lo_ss(xp[7], e2, acc[g7]);
+        acc[g8] = dp2a_hi_ss(xp[8], e2, acc[g8]);
+    }
+    acc[g4] = dp2a_lo_ss(xp[4], e3, acc[g4]);
+    acc[g9] = dp2a_hi_ss(xp[9], e3, acc[g9]);
+}
+
+// The five fp16 scales of a unit as floats: three words from the 4-byte aligned address
+// a + D, shifted right by sh bits (0, or 16 when the unit starts mid-word).
+template <int D>
+TQ_DEVFN void unit_scales(uint32_t a, uint32_t sh, float (&s)[5]) {
+    const uint32_t w0 = lds_w<D>(a), w1 = lds_w<D + 4>(a), w2 = lds_w<D + 8>(a);
+    const uint32_t v0 = __funnelshift_r(w0, w1, sh), v1 = __funnelshift_r(w1, w2, sh), v2 = w2 >> sh;
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v0));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v1));
+    s[0] = f0.x;
+    s[1] = f0.y;
+    s[2] = f1.x;
+    s[3] = f1.y;
+    s[4] = __low2float(*reinterpret_cast<const __half2*>(&v2));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritParams tp, const __grid_constant__ TritMaps maps) {
+    constexpr int G = 16;
+    using F = TritFmt<G>;
+    constexpr int GPU = 5, S = kTcS, US = kTcUS, D = kTcDepth, NC = kTcWarps, RT = kTcRows;
+    constexpr int NCT = NC * 32;  // consumer threads
+    static_assert(F::kUW == 4 && F::kGPU == GPU, "group 16 units");
+    const QmvParams& p = tp.q;
+    const int nst = tp.nsteps;
+    const int nunits_pad = nst * S;
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const uint32_t raw_addr = smem_u32(smraw);
+    uint8_t* sm = smraw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzled boxes want 1024-byte alignment
+    uint8_t* ring_c = sm;                                               // [slots][2048]
+    uint8_t* ring_s = ring_c + kTcSlots * kTcCode;                      // [slots][1280]
+    uint32_t* lut = reinterpret_cast<uint32_t*>(ring_s + kTcSlots * kTcScale);  // [81][32] signed digits
+    float* red = reinterpret_cast<float*>(lut + 81 * 32);               // [32]
+    uint32_t* xb = reinterpret_cast<uint32_t*>(red + 32);               // [nunits_pad][US]
+    float* xsum = reinterpret_cast<float*>(xb + nunits_pad * US);       // [nunits_pad * 5, padded to 4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(xsum + (nunits_pad * GPU + 3) / 4 * 4);
+    uint64_t* empty = full + kTcSlots;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTcSlots);
+    int* tag = reinterpret_cast<int*>(empty + kTcSlots + 1);            // [slots]: (task << 8) | stage, or -1
+    float* rowsum = reinterpret_cast<float*>(tag + (kTcSlots + 3) / 4 * 4);  // [tasks of this CTA][RT]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
+    const int t_end = (int)((int64_t)(blockIdx.x + 1) * tp.total_tasks / gridDim.x);
+    const int tpi = tp.tasks_per_item;
+    const uint32_t ring_c_addr = smem_u32(ring_c), ring_s_addr = smem_u32(ring_s);
+    uint32_t uses = 0;  // stages this warp (consumer) or this lane's consumer (producer) has passed through its ring
+
+    auto vec_of = [&](int item) { return p.mode == kModeGather ? item / p.k : item; };
+    // Segments: maximal runs of this CTA's tasks whose items share one input vector.
+    auto seg_end = [&](int s0) {
+        const int vec = vec_of(s0 / tpi);
+        int s1 = min(t_end, (s0 / tpi + 1) * tpi);
+        while (s1 < t_end && vec_of(s1 / tpi) == vec) s1 = min(t_end, (s1 / tpi + 1) * tpi);
+        return s1;
+    };
+
+    if (warp == 0) {
+        // ---------------- producer: lane w fills consumer warp w's ring.  Stages are handed out
+        // in order to whichever consumers have a free slot, and each slot's tag says which
+        // stage it holds (-1: the segment is over).  No block-wide barrier is taken after this
+        // point: the rings order producer and consumers.
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.codes)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.scales)) : "memory");
+        for (int i = lane; i < kTcSlots; i += 32) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        if (lane == 0) *abort_flag = 0;
+        fence_mbar_init();
+        __syncwarp();
+        named_bar_arrive(2, kTcThreads);  // barriers ready
+        int cur_item = -1, e = 0;  // the expert id of the item last handed out by this lane
+        for (int s0 = t_begin; s0 < t_end && !*abort_flag;) {
+            const int s1 = seg_end(s0);
+            const int nunits_seg = (s1 - s0) * nst;
+            int next = 0;            // next stage of the segment to hand out (same in every lane)
+            bool done = lane >= NC;  // this lane's consumer has its end mark
+            long long t0 = clock64();
+            for (;;) {
+                if (__all_sync(kFull, done)) break;
+                const int slot = lane * D + (int)(uses % D);
+                const bool ready = !done && mbar_test(empty + slot, ((uses / D) & 1) ^ 1);
+                const unsigned rmask = __ballot_sync(kFull, ready);
+                if (ready) {
+                    const int j = next + __popc(rmask & ((1u << lane) - 1));
+                    if (j < nunits_seg) {
+                        const int tl = j / nst, stage = j - tl * nst, task = s0 + tl;
+                        const int item = task / tpi;
+                        if (item != cur_item) {  // an id past the bank reads zeros (and is reported)
+                            e = p.mode == kModeDense ? 0 : __ldg(p.ids + item);
+                            cur_item = item;
+                            if ((e < 0 || e >= p.experts) && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+                        }
+                        const int row0 = (task % tpi) * RT;
+                        tag[slot] = (tl << 8) | stage;
+                        mbar_expect_tx(full + slot, kTcCode + kTcScale);
+                        tma_load_3d(ring_c_addr + slot * kTcCode, &maps.codes, stage * S * 4, row0, e, full + slot);
+                        tma_load_3d(ring_s_addr + slot * kTcScale, &maps.scales, stage * S * GPU, row0, e, full + slot);
+                    } else {
+                        tag[slot] = -1;
+                        mbar_arrive(full + slot);
+                        done = true;
+                    }
+                    ++uses;
+                }
+                next += __popc(rmask);
+                if (rmask) {
+                    t0 = clock64();
+                } else {
+                    if (*abort_flag) break;
+                    if (clock64() - t0 > kWaitCycles) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            s0 = s1;
+        }
+        __syncthreads();  // every consumer is done
+        if (*abort_flag && lane < NC) {
+            // Stopped early: let the copies this lane issued land before the CTA exits.
+            if (lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_TIMEOUT);
+            for (uint32_t k = 0; k < (uses < D ? uses : (uint32_t)D); ++k) {
+                const uint32_t u = uses - 1 - k;  // the last D uses of this lane's slots
+                mbar_wait_drain(full + lane * D + (int)(u % D), (u / D) & 1);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int cw = warp - 1, ctid = tid - 32;
+    for (int i = ctid; i < 81 * 32; i += NCT) {
+        const int v = i >> 5;
+        lut[i] = (((uint32_t)(v / 27 - 1)) & 0xffu) | ((((uint32_t)((v / 9) % 3 - 1)) & 0xffu) << 8) |
+                 ((((uint32_t)((v / 3) % 3 - 1)) & 0xffu) << 16) | (((uint32_t)(v % 3 - 1)) << 24);
+    }
+    const float cmid = __ldg(p.centroids + 1), delta = __ldg(p.centroids + 2) - cmid;
+    if (ctid == 0 && p.err && fabsf((cmid - __ldg(p.centroids)) - delta) > 1e-6f * fabsf(delta))
+        atomicOr(p.err, TQ_DEVERR_BAD_BOOK);
+    const bool has_off = cmid != 0.f;  // uniform
+    // lane row lr takes rows rA = (lr >> 1) + 4 (lr & 1) and rA + 8, so the two rows a quarter
+    // warp reads differ in bit 2 and their swizzled 16-byte pieces fall in different bank halves
+    const int lr = lane >> 2, c = lane & 3;
+    const int rA = (lr >> 1) + 4 * (lr & 1);
+    const uint32_t coff0 = (uint32_t)(rA * 128 + ((c ^ rA) * 16));  // piece of unit c (unit c + 4: ^ 64)
+    const uint32_t soff = (uint32_t)(rA * 80 + ((10 * c) & ~3));    // row B: + 640
+    const uint32_t ssh = (uint32_t)(c & 1) * 16u;
+    const uint32_t xoff = smem_u32(xb) + (uint32_t)(c * US * 4);
+    const uint32_t lut_bias = smem_u32(lut + lane) - (0x4B400000u << 7);
+    int cur_vec = -1;
+    float yscale = 0.f;  // delta * xs of the current vector
+    named_bar_sync(2, kTcThreads);  // the producer has initialised the barriers
+
+    for (int s0 = t_begin; s0 < t_end && !*abort_flag;) {
+        const int s1 = seg_end(s0);
+        const int vec = vec_of(s0 / tpi);
+        for (int i = ctid; i < (s1 - s0) * RT; i += NCT) rowsum[i] = 0.f;
+        if (vec != cur_vec) {
+            // One scale for the vector: xs = max|x| / 32767, xq = rint(x / xs); pair word pp of
+            // word w of a unit holds the inputs of unit trits 20w + 19 - 2pp (low half) and
+            // 20w + 18 - 2pp (high half), zero past the last column.
+            const float* xv = p.x + (int64_t)vec * p.cols;
+            // the pair of columns (k, k + 1), k even, sits at pair word pp of word w of unit u
+            auto pair_at = [&](int k) {
+                const int u = k / F::kUT, tl = k - u * F::kUT, w = tl / 20;
+                return u * US + w * F::kXW + (18 - (tl - 20 * w)) / 2;
+            };
+            auto pack = [](int qlo, int qhi) { return ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16); };
+            constexpr int kV4 = 4;  // 16-byte input loads per thread when the vector fits
+            const int nv4 = p.cols >> 2;
+            if ((p.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(xv) & 15) == 0 && nv4 <= kV4 * NCT) {
+                float4 xr[kV4];
+                float mx = 0.f;
+#pragma unroll
+                for (int r = 0; r < kV4; ++r) {
+                    const int f = ctid + r * NCT;
+                    xr[r] = f < nv4 ? __ldg(reinterpret_cast<const float4*>(xv) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xr[r].x), fabsf(xr[r].y)), fmaxf(fabsf(xr[r].z), fabsf(xr[r].w))));
+                }
+#pragma unroll
+                for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+                if (lane == 0) red[cw] = mx;
+                named_bar_sync(1, NCT);
+                mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) mx = fmaxf(mx, red[i]);
+                const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+                yscale = delta * (mx / 32767.0f);
+#pragma unroll
+                for (int r = 0; r < kV4; ++r) {
+                    const int f = ctid + r * NCT;
+                    if (f < nv4) {
+                        xb[pair_at(4 * f)] = pack(__float2int_rn(xr[r].x * inv), __float2int_rn(xr[r].y * inv));
+                        xb[pair_at(4 * f + 2)] = pack(__float2int_rn(xr[r].z * inv), __float2int_rn(xr[r].w * inv));
+                    }
+                }
+                for (int k = p.cols + 2 * ctid; k < nunits_pad * F::kUT; k += 2 * NCT) xb[pair_at(k)] = 0u;  // past the row
+            } else {
+                float mx = 0.f;
+                for (int k = ctid; k < p.cols; k += NCT) mx = fmaxf(mx, fabsf(__ldg(xv + k)));
+#pragma unroll
+                for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+                if (lane == 0) red[cw] = mx;
+                named_bar_sync(1, NCT);
+                mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) mx = fmaxf(mx, red[i]);
+                const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+                yscale = delta * (mx / 32767.0f);
+                for (int k = 2 * ctid; k < nunits_pad * F::kUT; k += 2 * NCT) {
+                    const float lo = k < p.cols ? __ldg(xv + k) : 0.f, hi = k + 1 < p.cols ? __ldg(xv + k + 1) : 0.f;
+                    xb[pair_at(k)] = pack(__float2int_rn(lo * inv), __float2int_rn(hi * inv));
+                }
+            }
+            if (has_off) {
+                for (int g = ctid; g < nunits_pad * GPU; g += NCT) {
+                    float sum = 0.f;
+                    for (int k = g * G; k < min((g + 1) * G, p.cols); ++k) sum += __ldg(xv + k);
+                    xsum[g] = sum;
+                }
+            }
+            cur_vec = vec;
+        }
+        named_bar_sync(1, NCT);  // table, input blocks and row sums ready
+
+        auto consume = [&](auto off_c) {
+            constexpr bool OFF = decltype(off_c)::value;
+            uint32_t slot = cw * D + uses % D, par = (uses / D) & 1;
+            for (;;) {
+                if (!mbar_wait(full + slot, par, abort_flag)) break;
+                const int tg = tag[slot];
+                if (tg < 0) {  // end of the segment
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty + slot);
+                    ++uses;
+                    break;
+                }
+                const int cs = tg & 255;                        // stage within the task
+                float* rs = rowsum + (tg >> 8) * RT + rA;       // row sums of the task, row A
+                const uint32_t cbase = ring_c_addr + slot * kTcCode;
+                const uint32_t sbase = ring_s_addr + slot * kTcScale + soff;
+                const uint32_t xs = xoff + (uint32_t)(cs * S * US * 4);
+                float totA = 0.f, totB = 0.f, offA = 0.f, offB = 0.f;
+                // unit pass JU: unit c + 4 JU of the stage, rows A and B (a pass past the row
+                // decodes zero words against zero inputs and scales)
+                auto pass = [&](auto ju_c) {
+                    constexpr int JU = decltype(ju_c)::value;
+                    const uint32_t ca = cbase + (JU == 0 ? coff0 : (coff0 ^ 64u));
+                    uint32_t accA[GPU], accB[GPU];
+#pragma unroll
+                    for (int g = 0; g < GPU; ++g) accA[g] = accB[g] = 0x4B400000u;
+                    const uint4 qa = lds_v4<0>(ca), qb = lds_v4<1024>(ca);
+                    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+                    static_for<0, 4>([&](auto wi_c) {
+                        constexpr int wi = decltype(wi_c)::value;
+                        constexpr int xd = (JU * 4 * US + wi * F::kXW) * 4;
+                        const uint4 xa = lds_v4<xd>(xs), xc = lds_v4<xd + 16>(xs);
+                        const uint2 xe = lds_v2<xd + 32>(xs);
+                        const uint32_t xp[10] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w, xe.x, xe.y};
+                        trit_word_signed<wi>(wa[wi], xp, accA, lut_bias);
+                        trit_word_signed<wi>(wb[wi], xp, accB, lut_bias);
+                    });
+                    float sA[5], sB[5];
+                    unit_scales<JU * 40>(sbase, ssh, sA);
+                    unit_scales<JU * 40 + 640>(sbase, ssh, sB);
+#pragma unroll
+                    for (int g = 0; g < GPU; ++g) {
+                        totA = fmaf(sA[g], __uint_as_float(accA[g]) - 12582912.0f, totA);
+                        totB = fmaf(sB[g], __uint_as_float(accB[g]) - 12582912.0f, totB);
+                    }
+                    if (OFF) {
+                        const float* xg = xsum + (cs * S + c + 4 * JU) * GPU;
+#pragma unroll
+                        for (int g = 0; g < GPU; ++g) {
+                            offA = fmaf(sA[g], xg[g], offA);
+                            offB = fmaf(sB[g], xg[g], offB);
+                        }
+                    }
+                };
+                pass(std::integral_constant<int, 0>{});
+                pass(std::integral_constant<int, 1>{});
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + slot);  // slot free for the producer
+                // this stage's partial row sums
+                float vA = OFF ? fmaf(yscale, totA, cmid * offA) : yscale * totA;
+                float vB = OFF ? fmaf(yscale, totB, cmid * offB) : yscale * totB;
+                vA += __shfl_xor_sync(kFull, vA, 1);
+                vB += __shfl_xor_sync(kFull, vB, 1);
+                vA += __shfl_xor_sync(kFull, vA, 2);
+                vB += __shfl_xor_sync(kFull, vB, 2);
+                if (c == 0) {
+                    atomicAdd(rs, vA);
+                    atomicAdd(rs + 8, vB);
+                }
+                ++uses;
+                if (++slot == (uint32_t)(cw * D + D)) {
+                    slot = cw * D;
+                    par ^= 1u;
+                }
+            }
+        };
+        if (has_off) consume(std::true_type{}); else consume(std::false_type{});
+        named_bar_sync(1, NCT);  // all row sums of the segment complete
+        for (int i = ctid; i < (s1 - s0) * RT; i += NCT) {
+            const int t = s0 + i / RT, row = (t % tpi) * RT + i % RT;
+            if (row < p.rows) store_from_float(p.y, (int64_t)(t / tpi) * p.rows + row, p.ydt, rowsum[i]);
+        }
+        named_bar_sync(1, NCT);  // row sums read out before the next segment clears them
+        s0 = s1;
+    }
+    __syncthreads();  // the producer drains its copies on an abort before the CTA exits
+}
+
+size_t trit_tc_smem(int nsteps, int max_tasks) {
+    const size_t nunits_pad = (size_t)nsteps * kTcS;
+    return 1024 + (size_t)kTcSlots * (kTcCode + kTcScale) + 4 * ((size_t)81 * 32 + 32) + 4 * nunits_pad * kTcUS +
+           4 * ((nunits_pad * 5 + 3) / 4 * 4) + 8 * (size_t)(2 * kTcSlots + 1) + 4 * (size_t)((kTcSlots + 3) / 4 * 4) +
+           4 * (size_t)max_tasks * kTcRows;
+}
+
+// Tensor maps of the code and scale banks (3-D: experts x rows x row).
+bool encode_trit_maps(const QmvParams& qp, TritMaps& m) {
+    const EncodeFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t ne = qp.mode == kModeDense ? 1 : qp.experts;
+    const int64_t esw = ne > 1 ? qp.expert_stride_w : (int64_t)qp.rows * qp.row_stride;
+    const int64_t ess = ne > 1 ? qp.expert_stride_s : (int64_t)qp.rows * qp.ngroups;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)qp.row_stride, (cuuint64_t)qp.rows, (cuuint64_t)ne};
+        const cuuint64_t strides[2] = {(cuuint64_t)qp.row_stride * 4, (cuuint64_t)esw * 4};
+        const cuuint32_t box[3] = {32, (cuuint32_t)kTcRows, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&m.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(qp.codes), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)qp.ngroups, (cuuint64_t)qp.rows, (cuuint64_t)ne};
+        const cuuint64_t strides[2] = {(cuuint64_t)qp.ngroups * 2, (cuuint64_t)ess * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)(kTcS * 5), (cuuint32_t)kTcRows, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&m.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(qp.scales), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+// Group 16 with tensor-copyable banks: 16-byte aligned bases, rows and experts a
+// multiple of 16 bytes apart.
+bool trit_tc_ok(const QmvParams& qp, int group) {
+    const bool dense = qp.mode == kModeDense || qp.experts <= 1;
+    return group == 16 && qp.rows > 0 && qp.cols > 0 && qp.row_stride % 4 == 0 && qp.ngroups % 8 == 0 &&
+           (dense || (qp.expert_stride_w % 4 == 0 && qp.expert_stride_s % 8 == 0)) &&
+           (reinterpret_cast<uintptr_t>(qp.codes) & 15) == 0 && (reinterpret_cast<uintptr_t>(qp.scales) & 15) == 0 &&
+           tensor_map_encoder() != nullptr;
+}
+
+tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st) {
+    using F = TritFmt<16>;
+    TritParams tp{};
+    tp.q = qp;
+    tp.units = (qp.cols + F::kUT - 1) / F::kUT;
+    tp.nsteps = (tp.units + kTcS - 1) / kTcS;
+    tp.tasks_per_item = (qp.rows + kTcRows - 1) / kTcRows;
+    tp.n_items = n_items;
+    const int64_t total = (int64_t)n_items * tp.tasks_per_item;
+    if (total > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    tp.total_tasks = (int)total;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    // one CTA per SM, fewer when there are fewer (task, stage) units than consumer warps
+    const int64_t work = total * tp.nsteps;
+    int64_t grid = std::min<int64_t>(sms, (work + kTcWarps - 1) / kTcWarps);
+    if (grid < (total + 255) / 256) grid = (total + 255) / 256;  // row-sum buffer: at most 256 tasks per CTA
+    if (grid < 1) grid = 1;
+    if (grid > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    const int max_tasks = (int)((total + grid - 1) / grid) + 1;
+    const size_t smem = trit_tc_smem(tp.nsteps, max_tasks);
+    if (smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
+    TritMaps maps;
+    if (!encode_trit_maps(qp, maps)) return TQ_ERR_UNSUPPORTED;
+    const void* kfn = (const void*)qmv_trit_tc_kernel;
+    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    qmv_trit_tc_kernel<<<(unsigned)grid, kTcThreads, smem, st>>>(tp, maps);
+    return launch_status();
+}
+
 }  // namespace
 
 // Rows per warp step: 4 rows x 8 units when a row holds many units, else 8 rows
@@ -656,7 +1178,14 @@ tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t 
     const bool pipe_ok = (group == 16 || group == 32) && ((int64_t)p.ngroups * 2) % 16 == 0 && p.row_stride < (1 << 30) &&
                          (p.expert_stride_s * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 &&
                          (reinterpret_cast<uintptr_t>(p.codes) & 15) == 0;
-    if (pipe_ok) return group == 16 ? launch_trit_pipe<16>(p, n_items, st) : launch_trit_pipe<32>(p, n_items, st);
+    if (pipe_ok) {
+        // group 16: the tensor-copy pipeline when the banks can be described by tensor maps
+        if (trit_tc_ok(p, group)) {
+            const tq_status s = launch_trit_tc(p, n_items, st);
+            if (s != TQ_ERR_UNSUPPORTED) return s;
+        }
+        return group == 16 ? launch_trit_pipe<16>(p, n_items, st) : launch_trit_pipe<32>(p, n_items, st);
+    }
     const int ut = 20 / std::gcd(20, group) * group;
     const bool wide = (p.cols + ut - 1) / ut >= 48;
     switch (group) {
