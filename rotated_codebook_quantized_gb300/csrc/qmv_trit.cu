@@ -732,6 +732,13 @@ struct TritMaps {
     CUtensorMap scales;  // [experts][rows][ngroups] fp16, box 40 x 16 x 1
 };
 
+// The 64-bit pair (v, v) of fp32 lanes.
+TQ_DEVFN uint64_t f32x2_splat(float v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+    return r;
+}
+
 // One 20-trit word against its 20 quantized inputs (pair words xp), added into the
 // unit's five group accumulators.  W is the word's index in the unit.
 template <int W>
@@ -739,14 +746,21 @@ TQ_DEVFN void trit_word_signed(uint32_t word, const uint32_t (&xp)[10], uint32_t
     constexpr int G = 16;
     const uint32_t hh = word / 59049u;
     const uint32_t ll = word - hh * 59049u;
+    // Both halves' digit steps at once, as pairs of fp32 lanes (same arithmetic, lane by lane).
     float t1[2], t2[2], b2[2];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const float hb = __uint_as_float((half == 0 ? hh : ll) | 0x4B000000u) - 8388972.0f;
-        t1[half] = fmaf(hb, 1.0f / 729.0f, 12582912.0f);
-        const float b1 = fmaf(t1[half] - 12582912.0f, -729.0f, hb);
-        t2[half] = fmaf(b1, 1.0f / 9.0f, 12582952.0f);
-        b2[half] = fmaf(t2[half] - 12582912.0f, -9.0f, b1);
+    {
+        uint64_t H, hb, T1, D1, B1, T2, D2, B2;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(H) : "r"(hh | 0x4B000000u), "r"(ll | 0x4B000000u));
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(hb) : "l"(H), "l"(f32x2_splat(-8388972.0f)));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(T1) : "l"(hb), "l"(f32x2_splat(1.0f / 729.0f)), "l"(f32x2_splat(12582912.0f)));
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(D1) : "l"(T1), "l"(f32x2_splat(-12582912.0f)));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(B1) : "l"(D1), "l"(f32x2_splat(-729.0f)), "l"(hb));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(T2) : "l"(B1), "l"(f32x2_splat(1.0f / 9.0f)), "l"(f32x2_splat(12582952.0f)));
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(D2) : "l"(T2), "l"(f32x2_splat(-12582912.0f)));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(B2) : "l"(D2), "l"(f32x2_splat(-9.0f)), "l"(B1));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(t1[0]), "=f"(t1[1]) : "l"(T1));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(t2[0]), "=f"(t2[1]) : "l"(T2));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(b2[0]), "=f"(b2[1]) : "l"(B2));
     }
     const float t3 = fmaf(b2[0], 9.0f, b2[1] + 12586552.0f);
     const uint32_t e3 = lds_u32(lut_bias + (__float_as_uint(t3) << 7));
@@ -833,6 +847,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
         // in order to whichever consumers have a free slot, and each slot's tag says which
         // stage it holds (-1: the segment is over).  No block-wide barrier is taken after this
         // point: the rings order producer and consumers.
+        int cur_item = -1, e = 0;  // the expert id of the item last handed out by this lane
+        if (t_begin < t_end && p.mode != kModeDense) {  // in flight while the barriers are set up
+            cur_item = t_begin / tpi;
+            e = __ldg(p.ids + cur_item);
+            if ((e < 0 || e >= p.experts) && p.err && lane == 0) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+        }
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.codes)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.scales)) : "memory");
         for (int i = lane; i < kTcSlots; i += 32) {
@@ -843,7 +863,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
         fence_mbar_init();
         __syncwarp();
         named_bar_arrive(2, kTcThreads);  // barriers ready
-        int cur_item = -1, e = 0;  // the expert id of the item last handed out by this lane
         for (int s0 = t_begin; s0 < t_end && !*abort_flag;) {
             const int s1 = seg_end(s0);
             const int nunits_seg = (s1 - s0) * nst;
@@ -905,6 +924,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
 
     // ---------------- consumers
     const int cw = warp - 1, ctid = tid - 32;
+    if (t_begin < t_end) {  // start fetching the first input vector while the table is built
+        const char* x0 = reinterpret_cast<const char*>(p.x + (int64_t)vec_of(t_begin / tpi) * p.cols);
+        for (int off = ctid * 128; off < p.cols * 4; off += NCT * 128)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(x0 + off));
+    }
     for (int i = ctid; i < 81 * 32; i += NCT) {
         const int v = i >> 5;
         lut[i] = (((uint32_t)(v / 27 - 1)) & 0xffu) | ((((uint32_t)((v / 9) % 3 - 1)) & 0xffu) << 8) |
@@ -1003,7 +1027,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             constexpr bool OFF = decltype(off_c)::value;
             uint32_t slot = cw * D + uses % D, par = (uses / D) & 1;
             for (;;) {
-                if (!mbar_wait(full + slot, par, abort_flag)) break;
+                if (!mbar_wait_short(full + slot, par, abort_flag)) break;
                 const int tg = tag[slot];
                 if (tg < 0) {  // end of the segment
                     __syncwarp();

@@ -68,6 +68,22 @@ TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) 
     return true;
 }
 
+// The same bounded wait, polling with short sleeps (for waits expected to be brief, where a
+// long suspension would outlast the event).
+TQ_DEVFN bool mbar_wait_short(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_test(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(b, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
 TQ_DEVFN void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Makes barrier initialisation visible to the async proxy (tensor copies).
