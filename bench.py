@@ -485,7 +485,7 @@ def main():
     k_ms = sum(kt) / len(kt)
     k_bytes = TOPK * gu_b
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    roofline = {"kernel": "qmv_trit_pipe_kernel<16> (gate||up gather_qmv, 8 ternary experts)", "bound": "hbm",
+    roofline = {"kernel": "qmv_trit_tc_kernel (gate||up gather_qmv, 8 ternary experts)", "bound": "hbm",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
                 "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_ms * 1e3}
