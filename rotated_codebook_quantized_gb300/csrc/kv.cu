@@ -187,6 +187,274 @@ __global__ void __launch_bounds__(32) kv_merge_kernel(const float* __restrict__ 
     for (int j = 0; j < 4; ++j) out[(int64_t)hq * kD + lane * 4 + j] = v[j] * r * (float)signs[lane * 4 + j];
 }
 
+// ---------------------------------------------------------------- 8-bit keys, group 32
+//
+// Same split-context layout, built for the cache the pages describe (8-bit keys
+// with a 256-level book, 3- or 4-bit values, groups of 32):
+//  * scores: a lane owns two tokens of the chunk and reads their key rows (128
+//    bytes each) with 16-byte loads; a code indexes a per-lane copy of the
+//    256-entry book in shared memory, and the rotated query of every head is a
+//    broadcast load per dimension; a group's partial sums are scaled once;
+//  * weighted values: a lane owns 8 dimensions for every token of its half warp,
+//    the row's codes arrive with one 64-bit funnel shift (3-bit words hold 10
+//    codes in bits 0..29, so word b shifted left by 30 continues word a), and
+//    p * s_v is formed once per token and head.
+constexpr int kGroupF = 32;
+
+TQ_DEVFN void cp_async16_kv(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+TQ_DEVFN void cp_async4_kv(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+
+template <int VL, int GQ>
+struct KvFast {
+    static constexpr int kVB = VL == 8 ? 3 : 4;        // value bits
+    static constexpr int kVCW = VL == 8 ? 10 : 8;      // value codes per word
+    static constexpr int kVW = (kD + kVCW - 1) / kVCW;  // value words per token
+    static constexpr size_t kVStage = (size_t)kChunk * kVW * 4 + (size_t)kChunk * 4 * 2;  // value codes + scales
+    static constexpr size_t kSmem =
+        sizeof(float) * (256 * 32 + (size_t)kD * GQ + (size_t)GQ * kChunk + (size_t)GQ * kD + 16 + 2 * GQ) + kVStage;
+};
+
+template <int VL, int GQ>
+__global__ void __launch_bounds__(kThreads, 2) kv_partial8_kernel(
+    const void* __restrict__ q, int qdt, int Hkv, int64_t ctx, int64_t capacity, const int8_t* __restrict__ signs,
+    const float* __restrict__ kcent, const float* __restrict__ vcent, const uint32_t* __restrict__ kcodes,
+    const uint16_t* __restrict__ kscales, const uint32_t* __restrict__ vcodes, const uint16_t* __restrict__ vscales,
+    float* __restrict__ part) {
+    using V = KvFast<VL, GQ>;
+    constexpr int NG = kD / kGroupF;  // 4 groups per row
+    extern __shared__ __align__(16) float smf[];
+    float* klut = smf;                   // [256][32]: entry c of lane l at c * 32 + l
+    float* qs = klut + 256 * 32;         // [kD][GQ]: rotated query / sqrt(D), per dimension
+    float* sc = qs + kD * GQ;            // [GQ][kChunk]: scores, then probabilities
+    float* obuf = sc + GQ * kChunk;      // [GQ][kD]
+    float* vlut = obuf + GQ * kD;        // [16]
+    float* stat = vlut + 16;             // [GQ][2]
+    uint32_t* vstage = reinterpret_cast<uint32_t*>(stat + 2 * GQ);                 // [kChunk][kVW] value codes
+    uint16_t* vsstage = reinterpret_cast<uint16_t*>(vstage + kChunk * V::kVW);   // [kChunk][4] value scales
+
+    const int h = blockIdx.x, split = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)split * kChunk;
+    const int n = (int)min((int64_t)kChunk, ctx - t0);
+
+    {
+        // the chunk's value codes and scales stream into shared memory during the scores
+        const uint32_t* vsrc = vcodes + ((int64_t)h * capacity + t0) * V::kVW;
+        const uint16_t* vssrc = vscales + ((int64_t)h * capacity + t0) * NG;
+        const int vwords = n * V::kVW, vsw = n * NG / 2;  // NG = 4 halves per token: whole words
+        if (((reinterpret_cast<uintptr_t>(vsrc) | reinterpret_cast<uintptr_t>(vstage)) & 15) == 0) {
+            for (int i = threadIdx.x; i < vwords / 4; i += kThreads) cp_async16_kv(vstage + 4 * i, vsrc + 4 * i);
+            for (int i = vwords / 4 * 4 + threadIdx.x; i < vwords; i += kThreads) cp_async4_kv(vstage + i, vsrc + i);
+        } else {
+            for (int i = threadIdx.x; i < vwords; i += kThreads) cp_async4_kv(vstage + i, vsrc + i);
+        }
+        const uint32_t* vss32 = reinterpret_cast<const uint32_t*>(vssrc);
+        for (int i = threadIdx.x; i < vsw; i += kThreads) cp_async4_kv(reinterpret_cast<uint32_t*>(vsstage) + i, vss32 + i);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < 256 * 32; i += kThreads) klut[i] = __ldg(kcent + (i >> 5));
+    for (int i = threadIdx.x; i < GQ * kD; i += kThreads) obuf[i] = 0.f;
+    if (threadIdx.x < VL) vlut[threadIdx.x] = __ldg(vcent + threadIdx.x);
+    // q_rot = H diag(s) q / sqrt(D), and the 1/sqrt(D) of the scores folded in.
+    for (int g = warp; g < GQ; g += kThreads / 32) {
+        const int hq = h * GQ + g;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = load_as_float(q, (int64_t)hq * kD + lane * 4 + i, qdt) * (float)signs[lane * 4 + i];
+        fwht_warp128(v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[(lane * 4 + i) * GQ + g] = v[i] * (1.0f / 128.0f);  // (1/sqrt(128))^2
+    }
+    __syncthreads();
+
+    // ---- scores: lane takes tokens i and i + 32 of each 64-token slice of its warp
+    const float* kl = klut + lane;
+    const uint4* kbase = reinterpret_cast<const uint4*>(kcodes + ((int64_t)h * capacity + t0) * (kD / 4));
+    const uint2* ksbase = reinterpret_cast<const uint2*>(kscales + ((int64_t)h * capacity + t0) * NG);
+    for (int i0 = warp * 64; i0 < n; i0 += (kThreads / 32) * 64) {
+        const int ia = i0 + lane, ib = i0 + 32 + lane;
+        const bool va = ia < n, vb = ib < n;
+        const uint4* ra = kbase + (int64_t)(va ? ia : 0) * 8;
+        const uint4* rb = kbase + (int64_t)(vb ? ib : 0) * 8;
+        const uint2 sa2 = va ? __ldg(ksbase + ia) : make_uint2(0u, 0u);
+        const uint2 sb2 = vb ? __ldg(ksbase + ib) : make_uint2(0u, 0u);
+        float tota[GQ], totb[GQ];
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) tota[g] = totb[g] = 0.f;
+        // a group's two 16-byte loads per row are in flight while the previous group is decoded
+        uint4 na[2], nb[2];
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            na[hc] = va ? __ldg(ra + hc) : make_uint4(0u, 0u, 0u, 0u);
+            nb[hc] = vb ? __ldg(rb + hc) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll 1
+        for (int grp = 0; grp < NG; ++grp) {
+            float pa[GQ], pb[GQ];
+#pragma unroll
+            for (int g = 0; g < GQ; ++g) pa[g] = pb[g] = 0.f;
+            const uint4 ca[2] = {na[0], na[1]}, cb[2] = {nb[0], nb[1]};
+            if (grp + 1 < NG) {
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    na[hc] = va ? __ldg(ra + (grp + 1) * 2 + hc) : make_uint4(0u, 0u, 0u, 0u);
+                    nb[hc] = vb ? __ldg(rb + (grp + 1) * 2 + hc) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {  // 16 dimensions per 16-byte load
+                const int c = grp * 2 + hc;
+                const uint4 wa = ca[hc];
+                const uint4 wb = cb[hc];
+                const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, bw[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int d = c * 16 + w * 4 + b;
+                        const float ka = kl[((aw[w] >> (8 * b)) & 255u) * 32];
+                        const float kb = kl[((bw[w] >> (8 * b)) & 255u) * 32];
+                        float qd[GQ];
+                        if constexpr (GQ % 4 == 0) {
+#pragma unroll
+                            for (int g = 0; g < GQ; g += 4) {
+                                const float4 q4 = *reinterpret_cast<const float4*>(qs + d * GQ + g);
+                                qd[g] = q4.x;
+                                qd[g + 1] = q4.y;
+                                qd[g + 2] = q4.z;
+                                qd[g + 3] = q4.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < GQ; ++g) qd[g] = qs[d * GQ + g];
+                        }
+#pragma unroll
+                        for (int g = 0; g < GQ; ++g) {
+                            pa[g] = fmaf(ka, qd[g], pa[g]);
+                            pb[g] = fmaf(kb, qd[g], pb[g]);
+                        }
+                    }
+                }
+            }
+            const uint32_t swa = grp < 2 ? sa2.x : sa2.y, swb = grp < 2 ? sb2.x : sb2.y;
+            const float sa = half_bits_to_float((uint16_t)(swa >> (16 * (grp & 1))));
+            const float sb = half_bits_to_float((uint16_t)(swb >> (16 * (grp & 1))));
+#pragma unroll
+            for (int g = 0; g < GQ; ++g) {
+                tota[g] = fmaf(sa, pa[g], tota[g]);
+                totb[g] = fmaf(sb, pb[g], totb[g]);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) {
+            if (va) sc[g * kChunk + ia] = tota[g];
+            if (vb) sc[g * kChunk + ib] = totb[g];
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's value copies
+    __syncthreads();                                       // everyone's, and the scores
+
+    // ---- chunk max and sum per head (warp g handles head g)
+    for (int g = warp; g < GQ; g += kThreads / 32) {
+        float m = -INFINITY;
+        for (int i = lane; i < n; i += 32) m = fmaxf(m, sc[g * kChunk + i]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        float l = 0.f;
+        for (int i = lane; i < n; i += 32) {
+            const float pr = expf(sc[g * kChunk + i] - m);
+            sc[g * kChunk + i] = pr;
+            l += pr;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+        if (lane == 0) {
+            stat[2 * g] = m;
+            stat[2 * g + 1] = l;
+        }
+    }
+    __syncthreads();
+
+    // ---- weighted sum of rotated values: half warp per token, lane owns dims 8 dl .. 8 dl + 7
+    const int half = lane >> 4, dl = lane & 15;
+    const int vgrp = (8 * dl) / kGroupF;
+    const int wlo = (8 * dl) / V::kVCW, whi = (8 * dl + 7) / V::kVCW;
+    const int vstart = V::kVB * ((8 * dl) % V::kVCW);
+    float o[GQ][8];
+#pragma unroll
+    for (int g = 0; g < GQ; ++g)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[g][j] = 0.f;
+    for (int i = warp * 2 + half; i < n; i += (kThreads / 32) * 2) {
+        const uint32_t* vr = vstage + i * V::kVW;
+        uint32_t bits;
+        if constexpr (V::kVB == 3) {
+            const uint64_t c64 = (uint64_t)vr[wlo] | ((uint64_t)vr[whi] << 30);
+            bits = (uint32_t)(c64 >> vstart);
+        } else {
+            bits = vr[dl];
+        }
+        const float s = half_bits_to_float(vsstage[i * NG + vgrp]);
+        float cv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cv[j] = vlut[(bits >> (V::kVB * j)) & (VL - 1)];
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) {
+            const float pw = sc[g * kChunk + i] * s;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[g][j] = fmaf(pw, cv[j], o[g][j]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < GQ; ++g)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float v = o[g][j] + __shfl_xor_sync(kFull, o[g][j], 16);
+            if (half == 0) atomicAdd(obuf + g * kD + 8 * dl + j, v);
+        }
+    __syncthreads();
+    // part[(split * Hq + hq) * (D + 2)] = {m, l, o[0..D)}
+    for (int idx = threadIdx.x; idx < GQ * kD; idx += kThreads) {
+        const int g = idx / kD, d = idx % kD;
+        const int hq = h * GQ + g;
+        float* dst = part + ((int64_t)split * Hkv * GQ + hq) * (kD + 2);
+        dst[2 + d] = obuf[idx];
+        if (d == 0) {
+            dst[0] = stat[2 * g];
+            dst[1] = stat[2 * g + 1];
+        }
+    }
+}
+
+template <int VL>
+tq_status launch_kv8(int gq, dim3 grid, cudaStream_t st, const void* q, int qdt, int Hkv, int64_t ctx,
+                     int64_t capacity, const int8_t* signs, const float* kc, const float* vc, const uint32_t* kcodes,
+                     const uint16_t* kscales, const uint32_t* vcodes, const uint16_t* vscales, float* part) {
+#define TQ_KV8_GQ(G)                                                                                           \
+    case G: {                                                                                                  \
+        const void* fn = (const void*)kv_partial8_kernel<VL, G>;                                              \
+        if (ensure_smem(fn, KvFast<VL, G>::kSmem) != cudaSuccess) return TQ_ERR_CUDA;                          \
+        kv_partial8_kernel<VL, G><<<grid, kThreads, KvFast<VL, G>::kSmem, st>>>(                               \
+            q, qdt, Hkv, ctx, capacity, signs, kc, vc, kcodes, kscales, vcodes, vscales, part);                \
+        break;                                                                                                 \
+    }
+    switch (gq) {
+        TQ_KV8_GQ(1)
+        TQ_KV8_GQ(2)
+        TQ_KV8_GQ(4)
+        TQ_KV8_GQ(8)
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+#undef TQ_KV8_GQ
+    return launch_status();
+}
+
 template <int KL, int VL>
 tq_status launch_kv(int gq, dim3 grid, cudaStream_t st, const void* q, int qdt, int Hkv, int64_t ctx, int64_t capacity,
                     const int8_t* signs, const float* kc, const float* vc, int group, const uint32_t* kcodes,
@@ -237,7 +505,16 @@ extern "C" tq_status tq_kv_attend(const void* q, tq_dtype qdt, int32_t Hq, int32
     const dim3 grid(Hkv, (unsigned)nsplit);
     tq_status s;
     const int kl = kcb->levels, vl = vcb->levels;
-    if (kl == 256 && vl == 8)
+    // 8-bit keys in groups of 32 with 16-byte aligned key rows: the kernel above
+    const bool k8 = kl == 256 && (vl == 8 || vl == 16) && group == kGroupF &&
+                    (reinterpret_cast<uintptr_t>(kcodes) & 15) == 0 && (reinterpret_cast<uintptr_t>(kscales) & 7) == 0 &&
+                    (reinterpret_cast<uintptr_t>(vcodes) & 3) == 0 && (reinterpret_cast<uintptr_t>(vscales) & 3) == 0;
+    if (k8)
+        s = vl == 8 ? launch_kv8<8>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids,
+                                    vcb->centroids, kcodes, kscales, vcodes, vscales, part)
+                    : launch_kv8<16>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids,
+                                     vcb->centroids, kcodes, kscales, vcodes, vscales, part);
+    else if (kl == 256 && vl == 8)
         s = launch_kv<256, 8>(gq, grid, st, q, qdt, Hkv, ctx, capacity, rot->signs, kcb->centroids, vcb->centroids,
                               group, kcodes, kscales, vcodes, vscales, part, (int)nsplit);
     else if (kl == 16 && vl == 16)
