@@ -188,11 +188,12 @@ TQ_DEVFN void fwht_warp128(float (&v)[4]) {
     v[3] = a1 - a3;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = lane & m;
+        // the upper lane of a pair keeps o - v, the lower v + o: one fma with a sign of +-1 (exact)
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float o = __shfl_xor_sync(kFull, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
+            const float o = __shfl_xor_sync(kFull, v[i], m);
+            v[i] = fmaf(sgn, v[i], o);
         }
     }
 }

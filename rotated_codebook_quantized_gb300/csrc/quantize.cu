@@ -7,6 +7,9 @@
 // (20 base-3 trits per word for the three-level book, "The ternary tier").
 #include <math.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "common.cuh"
 
 using namespace tq;
@@ -171,6 +174,208 @@ __global__ void __launch_bounds__(256) kv_quantize_kernel(const void* __restrict
     }
 }
 
+// ---------------------------------------------------------------- KV vectors, 8-bit keys, group 32
+//
+// Persistent warps, one (token, kv head) vector pair (K and V) at a time, the next pair's
+// inputs in flight while the current one is encoded.  A lane holds dims 4l .. 4l+3, so an
+// 8-bit key word is exactly one lane's four codes.  The 255 key thresholds are looked up in
+// a table of 1024 equal bins over [-4.5, 4.5): bin(x) = floor((x + 4.5) * 1024 / 9), the
+// same float expression for the thresholds and for a value, so it is monotone in x.  The
+// book's thresholds are at least 0.0169 apart, wider than a bin (0.0088), so a bin holds at
+// most one; every threshold of a lower bin is below u, every one of a higher bin above, and
+// code = (thresholds of lower bins) + (the bin's own threshold < u) is exactly the count of
+// thresholds strictly below u.  Values are divided by the group scale through one
+// reciprocal per group (a code can differ from a correctly rounded division only at a tie).
+constexpr int kKvBins = 1024;
+constexpr int kKvVBins = 64;  // value books: 8 or 16 levels, thresholds >= 0.258 apart, bins 0.14 wide
+constexpr float kKvVBinScale = (float)kKvVBins / 9.0f;
+// vector pairs per warp ring: 8 of bf16 (4 KB), 4 of fp32 (4 KB)
+template <bool BF16>
+constexpr int kv_ring_len() { return BF16 ? 8 : 4; }
+
+// Pairs gw, gw + nw, ... below nvec.
+TQ_DEVFN int64_t vec0_count(int64_t gw, int64_t nw, int64_t nvec) { return gw < nvec ? (nvec - gw + nw - 1) / nw : 0; }
+constexpr float kKvLo = -4.5f, kKvBinScale = (float)kKvBins / 9.0f;
+
+template <int VL, bool BF16>
+__global__ void __launch_bounds__(256, 4) kv_quantize8_kernel(const void* __restrict__ k, const void* __restrict__ v,
+                                                           int64_t nvec, int Hkv, int64_t pos, int64_t capacity,
+                                                           float rscale, const int8_t* __restrict__ signs,
+                                                           const float* __restrict__ kthr, const float* __restrict__ vthr,
+                                                           uint32_t* __restrict__ kcodes, uint16_t* __restrict__ kscales,
+                                                           uint32_t* __restrict__ vcodes, uint16_t* __restrict__ vscales) {
+    constexpr int VB = VL == 8 ? 3 : 4, VCW = VL == 8 ? 10 : 8, VW = (128 + VCW - 1) / VCW;
+    __shared__ float2 bins[kKvBins];  // (count of thresholds of lower bins, the bin's threshold or +inf)
+    __shared__ float2 vbins[kKvVBins];
+    __shared__ float kt[256];
+    __shared__ int kb[256];
+    __shared__ float vt[16];
+    __shared__ int vb[16];
+    constexpr int kRing = kv_ring_len<BF16>();
+    __shared__ __align__(16) uint8_t kv_ring[8 * kRing * 2 * 128 * (BF16 ? 2 : 4)];  // [8 warps][kRing][pair]
+    auto bin_of = [](float x) { return min(max(__float2int_rd((x - kKvLo) * kKvBinScale), 0), kKvBins - 1); };
+    auto vbin_of = [](float x) { return min(max(__float2int_rd((x - kKvLo) * kKvVBinScale), 0), kKvVBins - 1); };
+    for (int i = threadIdx.x; i < 255; i += blockDim.x) {
+        kt[i] = __ldg(kthr + i);
+        kb[i] = bin_of(kt[i]);
+    }
+    if (threadIdx.x < VL - 1) {
+        vt[threadIdx.x] = __ldg(vthr + threadIdx.x);
+        vb[threadIdx.x] = vbin_of(vt[threadIdx.x]);
+    }
+    __syncthreads();
+    // bin b: (thresholds whose bin is below b, the one whose bin is b or +inf); the thresholds ascend
+    auto fill = [&](float2* tab, int nb, const float* t, const int* tb, int n) {
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            int lo = 0, hi = n;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (tb[mid] < b) lo = mid + 1; else hi = mid;
+            }
+            tab[b] = make_float2(__int_as_float(lo), lo < n && tb[lo] == b ? t[lo] : INFINITY);
+        }
+    };
+    fill(bins, kKvBins, kt, kb, 255);
+    fill(vbins, kKvVBins, vt, vb, VL - 1);
+    // A book whose thresholds share a bin (not a Gaussian Lloyd-Max book) is snapped by search.
+    const bool kfast = __syncthreads_and(threadIdx.x >= 254 || kb[threadIdx.x] < kb[threadIdx.x + 1]);
+    const bool vfast = __syncthreads_and(threadIdx.x >= VL - 2 || vb[threadIdx.x] < vb[threadIdx.x + 1]);
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t sg = __ldg(reinterpret_cast<const uint32_t*>(signs) + lane);  // signs of dims 4l .. 4l+3
+    float sgn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sgn[i] = (float)(int8_t)(sg >> (8 * i));
+
+    // Per-warp ring of kRing vector pairs in shared memory, filled with 16-byte cp.async copies
+    // (K then V, 32 lanes x ES / 2 copies per pair): kRing - 1 pairs in flight while one is encoded.
+    constexpr int ES = BF16 ? 2 : 4, PAIR = 2 * 128 * ES, CPL = PAIR / (32 * 16);
+    uint8_t* ring = kv_ring + (threadIdx.x >> 5) * kRing * PAIR;
+    const int64_t nmine = vec0_count(gw, nw, nvec);  // pairs of this warp: gw, gw + nw, ...
+    auto issue = [&](int64_t j) {  // pair j of this warp into slot j % kRing
+        if (j < nmine) {
+            const int64_t vec = gw + j * nw;
+            uint8_t* dst = ring + (j % kRing) * PAIR;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const int piece = lane + 32 * c;  // 16-byte piece of the pair
+                const int half = piece >= (PAIR / 32) ? 1 : 0;
+                const int off = piece * 16 - half * (PAIR / 2);
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(half ? v : k) + vec * (PAIR / 2) + off;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + piece * 16)),
+                             "l"(src)
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto read4 = [&](const uint8_t* src, float (&x)[4]) {  // this lane's dims 4l .. 4l+3
+        if (BF16) {
+            const uint2 r = *reinterpret_cast<const uint2*>(src + lane * 8);
+            x[0] = __uint_as_float(r.x << 16);
+            x[1] = __uint_as_float(r.x & 0xffff0000u);
+            x[2] = __uint_as_float(r.y << 16);
+            x[3] = __uint_as_float(r.y & 0xffff0000u);
+        } else {
+            const float4 r = *reinterpret_cast<const float4*>(src + lane * 16);
+            x[0] = r.x;
+            x[1] = r.y;
+            x[2] = r.z;
+            x[3] = r.w;
+        }
+    };
+    // rotate, then scale by the group RMS (8 lanes per group of 32): returns the fp16 scale bits
+    auto prep = [&](float (&x)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] *= sgn[i];
+        fwht_warp128(x);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] *= rscale;
+        float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+        ss += __shfl_xor_sync(kFull, ss, 1);
+        ss += __shfl_xor_sync(kFull, ss, 2);
+        ss += __shfl_xor_sync(kFull, ss, 4);
+        const float sc = sqrtf(ss * (1.0f / 32.0f));
+        const float inv = sc > 0.f ? 1.0f / sc : 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] *= inv;
+        return __half_as_ushort(__float2half_rn(sc));
+    };
+
+    // the encode loop, once with the bin tables and once (any other book) with searches
+    auto run = [&](auto fast_c) {
+    constexpr bool FAST = decltype(fast_c)::value;
+#pragma unroll 1
+    for (int j = 0; j < kRing - 1; ++j) issue(j);
+    // (token, head) of this warp's pair j, advanced by nw pairs per step without a division
+    int64_t tok = gw / Hkv;
+    int hh = (int)(gw - tok * Hkv);
+    const int64_t dtok = nw / Hkv;
+    const int dhh = (int)(nw - dtok * Hkv);
+    for (int64_t j = 0; j < nmine; ++j) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 2) : "memory");  // pair j has landed (this lane's pieces)
+        __syncwarp();                                                       // every lane's, and slot j - 1 is free
+        issue(j + kRing - 1);
+        const uint8_t* pr = ring + (j % kRing) * PAIR;
+        float kx[4], vx[4];
+        read4(pr, kx);
+        read4(pr + PAIR / 2, vx);
+        const int64_t slot = (int64_t)hh * capacity + pos + tok;
+        tok += dtok;
+        hh += dhh;
+        if (hh >= Hkv) {
+            hh -= Hkv;
+            ++tok;
+        }
+        const uint16_t ks = prep(kx), vs = prep(vx);
+        // keys: one word per lane
+        uint32_t kw = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float u = kx[i];
+            int c;
+            if constexpr (FAST) {
+                const float2 e = bins[bin_of(u)];
+                c = __float_as_int(e.x) + (e.y < u ? 1 : 0);
+            } else {
+                c = snap_code(u, kt, 255);
+            }
+            kw |= (uint32_t)c << (8 * i);
+        }
+        kcodes[slot * 32 + lane] = kw;
+        // values: lane's four codes, then word j gathers codes 10j .. 10j+9 (3-bit) or 8j .. 8j+7
+        uint32_t vc4 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int c;
+            if constexpr (FAST) {
+                const float2 e = vbins[vbin_of(vx[i])];
+                c = __float_as_int(e.x) + (e.y < vx[i] ? 1 : 0);
+            } else {
+                c = snap_code(vx[i], vt, VL - 1);
+            }
+            vc4 |= (uint32_t)c << (VB * i);
+        }
+        uint32_t vw = 0;
+        const int first = lane * VCW;  // first dim of word `lane`
+        const int src0 = min(first >> 2, 31);
+        const uint32_t a0 = __shfl_sync(kFull, vc4, src0), a1 = __shfl_sync(kFull, vc4, min(src0 + 1, 31)),
+                       a2 = __shfl_sync(kFull, vc4, min(src0 + 2, 31));
+        // the three lanes' 12 codes as one bit string, then the word's VCW codes from dim `first`
+        const uint64_t cat = (uint64_t)a0 | ((uint64_t)a1 << (4 * VB)) | ((uint64_t)a2 << (8 * VB));
+        vw = (uint32_t)(cat >> (VB * (first & 3)));
+        if (VCW * VB < 32) vw &= (1u << (VCW * VB)) - 1u;
+        if (lane == VW - 1 && 128 % VCW) vw &= (1u << (VB * (128 % VCW))) - 1u;  // last word: past dim 127 is 0
+        if (lane < VW) vcodes[slot * VW + lane] = vw;
+        // scales: lanes 0, 8, 16, 24 hold their group's
+        if ((lane & 7) == 0) {
+            kscales[slot * 4 + (lane >> 3)] = ks;
+            vscales[slot * 4 + (lane >> 3)] = vs;
+        }
+    }    };
+    if (kfast && vfast) run(std::true_type{}); else run(std::false_type{});
+}
+
 // Elements per thread: smallest power of two E with whole warps (dim % 32E == 0),
 // at most 1024 threads, E <= block, and a group spread over at most one warp
 // (group / E <= 32) so the group's sum of squares is a warp-shuffle reduction.
@@ -236,6 +441,32 @@ extern "C" tq_status tq_kv_quantize(const void* k, const void* v, tq_dtype dt, i
     if (!k || !v || !kcodes || !kscales || !vcodes || !vscales) return TQ_ERR_INVALID;
     const int kw = (int)tq_row_words(kcb->levels, D), vw = (int)tq_row_words(vcb->levels, D);
     const int64_t nvec = (int64_t)T * Hkv;
+    const float rscale = (float)(1.0 / sqrt((double)D));
+    // 8-bit keys, 3- or 4-bit values, groups of 32: the persistent kernel above
+    const uintptr_t need = 15;  // 16-byte copies of the inputs
+    if (kcb->levels == 256 && (vcb->levels == 8 || vcb->levels == 16) && group == 32 &&
+        ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & need) == 0 &&
+        (reinterpret_cast<uintptr_t>(rot->signs) & 3) == 0) {
+        static int sms = 0;
+        if (sms == 0) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        }
+        const int64_t blocks = std::min<int64_t>((nvec + 7) / 8, (int64_t)sms * 4);
+        cudaStream_t st = as_stream(stream);
+#define TQ_KV8(VL, BF)                                                                                            \
+    kv_quantize8_kernel<VL, BF><<<(unsigned)blocks, 256, 0, st>>>(k, v, nvec, Hkv, pos, capacity, rscale, rot->signs, \
+                                                                   kcb->thresholds, vcb->thresholds, kcodes, kscales,  \
+                                                                   vcodes, vscales)
+        if (vcb->levels == 8) {
+            if (dt == TQ_BF16) TQ_KV8(8, true); else TQ_KV8(8, false);
+        } else {
+            if (dt == TQ_BF16) TQ_KV8(16, true); else TQ_KV8(16, false);
+        }
+#undef TQ_KV8
+        return launch_status();
+    }
     const int warps = 8;
     const int64_t blocks = (nvec + warps - 1) / warps;
     if (blocks > 0x7fffffffll) return TQ_ERR_INVALID;
