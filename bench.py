@@ -2,8 +2,9 @@
 
 Workload: one MoE decode step = route 1 token over 384 experts (top-8, fp32
 logits), rotate its bf16 [1, 7168] input, gate||up gather-qmv over the 8
-routed ternary experts (group 16, 20 trits per word), SwiGLU + rotation of the
-2048-wide intermediate, down multi-gather-qmv, router-weighted combine.  The
+routed ternary experts (group 16, 20 trits per word), down multi-gather-qmv
+with the SwiGLU and the rotation of the 2048-wide intermediate done inside
+it, router-weighted combine.  The
 metric is packed-weight bytes read per second by the step (codes + fp16 scales
 of the 8 routed experts, 114,720,768 B per step).
 
@@ -414,11 +415,24 @@ def main():
         ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)  # decode reads experts by id
         xr = tq.rotate(x_buf, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
+        yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))  # SwiGLU + rotation inside
+        return tq.moe_combine(yd, probs, TOPK)
+
+    def step_all_fused():  # the input rotation inside gate||up too (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
+        gu = tq.gather_qmv_rotate(qgu, x_buf, rotH, ids)
+        yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))
+        return tq.moe_combine(yd, probs, TOPK)
+
+    def step_separate():  # six separate calls, one per hot-path step (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
+        xr = tq.rotate(x_buf, rotH)
+        gu = tq.gather_qmv(qgu, xr, ids)
         hr = tq.swiglu_rotate(gu, INTER, rotI)
         yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    launches_per_step = 6  # route top-k; rotate; gather; swiglu+rotate; multi-gather; combine (one kernel each)
+    launches_per_step = 5  # route top-k; rotate; gate||up gather; down multi-gather with SwiGLU; combine
 
     # warm up eagerly (first calls set kernel attributes), then capture the step
     logits_buf.copy_(logits_all[0:1])
@@ -528,6 +542,12 @@ def main():
            "ms_per_step": e2e_ms / args.steps}
 
     prefill = None if args.skip_prefill else measure_prefill(torch, tq, wl, dev, flush, peaks)
+    # the same step with other splits into calls (same inputs; one graph replay each, L2 flushed)
+    step_variants = None
+    if not args.skip_extras:
+        step_variants = {"headline_5_launches_us": graph_time_us(torch, step, flush),
+                         "separate_6_launches_us": graph_time_us(torch, step_separate, flush),
+                         "rotation_in_gate_up_too_4_launches_us": graph_time_us(torch, step_all_fused, flush)}
     extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
 
     if rank == 0:
@@ -537,7 +557,7 @@ def main():
                 "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "gather_qmm_tflops": prefill["value"] if prefill else None, "prefill": prefill,
-                "extras": extras, "wall_s_timed_loop": wall}
+                "extras": extras, "step_variants": step_variants, "wall_s_timed_loop": wall}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -187,6 +187,28 @@ tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t
 tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
                               void* y, tq_dtype ydt, uint32_t* err, void* stream);
 
+/* tq_gather_qmv with the input rotation done inside the matvec: y[t, j, :] =
+ * W_{ids[t, j]} (R x[t]), R = rot (blockdiag(H_block) diag(signs) / sqrt(block),
+ * "How it works": the input is rotated once per layer and shared by every
+ * expert).  x: device [T, cols] of xdt (f32 or bf16); rot->dim == cols.
+ * Saves the separate tq_rotate launch of a decode step.  Supported for
+ * three-level books with group 16 whose banks the tensor-copy kernel can read
+ * (16-byte aligned codes and scales, row and expert strides in whole 16-byte
+ * chunks, cols a multiple of 32, rot->block in 32..8192); TQ_ERR_UNSUPPORTED
+ * otherwise (then call tq_rotate and tq_gather_qmv). */
+tq_status tq_gather_qmv_rotate(const tq_qweight_t* w, const void* x, tq_dtype xdt, const tq_rotation_t* rot,
+                               const int32_t* ids, int32_t T, int32_t k, void* y, tq_dtype ydt, uint32_t* err,
+                               void* stream);
+
+/* tq_multi_gather_qmv with tq_swiglu_rotate folded in: y[p, :] = W_{ids[p]} h_rot[p]
+ * with h_rot[p] = R (silu(gate_up[p, 0:cols]) * gate_up[p, cols:2 cols]).
+ * gate_up: device f32 [P, 2 * cols] (an expert's gate | up outputs); rot->dim ==
+ * cols.  Same support as tq_gather_qmv_rotate; TQ_ERR_UNSUPPORTED otherwise
+ * (then call tq_swiglu_rotate and tq_multi_gather_qmv). */
+tq_status tq_multi_gather_qmv_swiglu(const tq_qweight_t* w, const float* gate_up, const tq_rotation_t* rot,
+                                     const int32_t* ids, int32_t P, void* y, tq_dtype ydt, uint32_t* err,
+                                     void* stream);
+
 /* Router: top-k experts per token, softmax weights, expert-sorted pair order.
  * "Running a 1T-Parameter Model on a Laptop": the router picks the 8 best of
  * 384 experts per token; "How it works", row "A large batch sorted by expert".

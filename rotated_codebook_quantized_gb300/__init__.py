@@ -56,6 +56,10 @@ _SIGS = {
     "tq_qmv": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p]),
     "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p]),
     "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
+    "tq_gather_qmv_rotate": (_i32, [_P(tq_qweight_t), _c_p, _i32, _P(tq_rotation_t), _c_p, _i32, _i32, _c_p, _i32,
+                                    _c_p, _c_p]),
+    "tq_multi_gather_qmv_swiglu": (_i32, [_P(tq_qweight_t), _c_p, _P(tq_rotation_t), _c_p, _i32, _c_p, _i32, _c_p,
+                                          _c_p]),
     "tq_moe_route": (_i32, [_c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _sz, _c_p]),
     "tq_route_workspace_bytes": (_sz, [_i32]),
     "tq_swiglu_rotate": (_i32, [_c_p, _i64, _i32, _P(tq_rotation_t), _c_p, _i32, _c_p]),
@@ -274,6 +278,32 @@ def multi_gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
     q = w.c()
     _check(load().tq_multi_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), P, _ptr(y), _dt(y), _ptr(err),
                                       _stream()), "tq_multi_gather_qmv")
+    return y
+
+
+def gather_qmv_rotate(w: QWeight, x, rot: Rotation, ids, out_dtype=None, err=None):
+    """gather_qmv of R x with the rotation done inside the matvec (x: f32 or bf16 [T, cols])."""
+    torch = _torch()
+    _contig(x, "x")
+    _contig(ids, "ids")
+    T, k = ids.shape
+    y = torch.empty((T, k, w.rows), dtype=out_dtype or torch.float32, device=x.device)
+    q, r = w.c(), rot.c()
+    _check(load().tq_gather_qmv_rotate(ctypes.byref(q), _ptr(x), _dt(x), ctypes.byref(r), _ptr(ids), T, k, _ptr(y),
+                                       _dt(y), _ptr(err), _stream()), "tq_gather_qmv_rotate")
+    return y
+
+
+def multi_gather_qmv_swiglu(w: QWeight, gate_up, rot: Rotation, ids, out_dtype=None, err=None):
+    """multi_gather_qmv of R (silu(gate) * up) per pair, SwiGLU and rotation inside (gate_up: f32 [P, 2*cols])."""
+    torch = _torch()
+    _contig(gate_up, "gate_up")
+    _contig(ids, "ids")
+    P = ids.shape[0]
+    y = torch.empty((P, w.rows), dtype=out_dtype or torch.float32, device=gate_up.device)
+    q, r = w.c(), rot.c()
+    _check(load().tq_multi_gather_qmv_swiglu(ctypes.byref(q), _ptr(gate_up), ctypes.byref(r), _ptr(ids), P, _ptr(y),
+                                             _dt(y), _ptr(err), _stream()), "tq_multi_gather_qmv_swiglu")
     return y
 
 

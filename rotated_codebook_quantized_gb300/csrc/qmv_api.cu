@@ -139,6 +139,40 @@ extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_r
     return run(p, w->group, 1, P, as_stream(stream));
 }
 
+extern "C" tq_status tq_gather_qmv_rotate(const tq_qweight_t* w, const void* x, tq_dtype xdt,
+                                          const tq_rotation_t* rot, const int32_t* ids, int32_t T, int32_t k,
+                                          void* y, tq_dtype ydt, uint32_t* err, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (T < 0 || k <= 0 || !ydt_ok(ydt) || (xdt != TQ_F32 && xdt != TQ_BF16)) return TQ_ERR_INVALID;
+    if (!rot || !rot->signs || rot->dim != w->cols) return TQ_ERR_INVALID;
+    if (T == 0) return TQ_OK;
+    if (!x || !ids || !y) return TQ_ERR_INVALID;
+    if (w->cb.levels != 3 || (int64_t)T * k > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
+    QmvParams p = make_params(w, nullptr, y, ydt, err);
+    p.mode = kModeGather;
+    p.ids = ids;
+    p.k = k;
+    return qmv_trit_xstage_run(p, w->group, T * k, 1, x, xdt, rot->signs, rot->block, as_stream(stream));
+}
+
+extern "C" tq_status tq_multi_gather_qmv_swiglu(const tq_qweight_t* w, const float* gate_up,
+                                               const tq_rotation_t* rot, const int32_t* ids, int32_t P, void* y,
+                                               tq_dtype ydt, uint32_t* err, void* stream) {
+    tq_status s = check_qweight(w);
+    if (s != TQ_OK) return s;
+    if (P < 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
+    if (!rot || !rot->signs || rot->dim != w->cols) return TQ_ERR_INVALID;
+    if (P == 0) return TQ_OK;
+    if (!gate_up || !ids || !y) return TQ_ERR_INVALID;
+    if (w->cb.levels != 3) return TQ_ERR_UNSUPPORTED;
+    QmvParams p = make_params(w, nullptr, y, ydt, err);
+    p.mode = kModeMulti;
+    p.ids = ids;
+    p.k = 1;
+    return qmv_trit_xstage_run(p, w->group, P, 2, gate_up, TQ_F32, rot->signs, rot->block, as_stream(stream));
+}
+
 // ---------------------------------------------------------------- dequant_experts
 
 namespace {

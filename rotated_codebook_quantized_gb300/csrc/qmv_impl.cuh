@@ -297,6 +297,11 @@ tq_status dispatch_qmv_nv(QmvParams p, int nv, int n_items, cudaStream_t st) {
 
 // Ternary books with one input vector per item (qmv_trit.cu).
 tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
+// The ternary tensor-copy kernel with an input stage: xmode 1 rotates rows of xin (dtype xdt),
+// xmode 2 takes rows [gate | up] of f32 xin, applies SwiGLU, then rotates.  TQ_ERR_UNSUPPORTED
+// where that kernel does not apply.
+tq_status qmv_trit_xstage_run(const QmvParams& p, int group, int n_items, int xmode, const void* xin, int xdt,
+                              const int8_t* signs, int block, cudaStream_t st);
 bool qmv_bits_ok(const QmvParams& p, int group);
 tq_status qmv_bits_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
 

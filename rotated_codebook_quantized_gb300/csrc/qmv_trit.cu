@@ -67,6 +67,13 @@ struct TritParams {
     int tasks_per_item;
     int n_items;
     int total_tasks;
+    // input stage of the tensor-copy kernel: 0 = q.x is the rotated input; 1 = xin rows are
+    // rotated here; 2 = xin rows are [gate | up] pairs, SwiGLU'd then rotated here
+    int xmode;
+    const void* xin;
+    int xdt;
+    const int8_t* xsigns;
+    int xblock;
 };
 
 template <int G, int RPW>
@@ -727,6 +734,71 @@ TQ_DEVFN void named_bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// M-point Hadamard transforms down the 32 columns of every block of M rows of a padded
+// [rows][33] float array (rows = a multiple of M; M a power of two up to 256).  A warp takes
+// 32 / L columns at a time, L = min(M, 32) lanes per column, each lane E = M / L elements
+// (rows i0 + L j): in-register butterflies over j, then shuffles over the lane bits.
+template <int M>
+TQ_DEVFN void hadamard_columns_m(float* xf, int nrows, int warp, int nwarps, int lane) {
+    constexpr int L = M < 32 ? M : 32, E = M / L, CPW = 32 / L;
+    constexpr int P = E >= 8 ? 1 : 8 / E;  // independent column groups per pass (ILP)
+    const int ncols = (nrows / M) * 32;     // (block, column) pairs
+    const int i0 = lane % L;
+    for (int cb = warp * CPW; cb < ncols; cb += P * nwarps * CPW) {
+        float e[P][E];
+        float* base[P];
+        bool on[P];
+#pragma unroll
+        for (int g = 0; g < P; ++g) {
+            const int col = cb + g * nwarps * CPW + lane / L;
+            on[g] = col < ncols;
+            const int blk = on[g] ? col >> 5 : 0, c = col & 31;
+            base[g] = xf + (blk * M + i0) * 33 + c;
+#pragma unroll
+            for (int j = 0; j < E; ++j) e[g][j] = on[g] ? base[g][L * j * 33] : 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < P; ++g)
+#pragma unroll
+            for (int st = 1; st < E; st <<= 1)
+#pragma unroll
+                for (int j = 0; j < E; ++j)
+                    if (!(j & st)) {
+                        const float x0 = e[g][j], x1 = e[g][j + st];
+                        e[g][j] = x0 + x1;
+                        e[g][j + st] = x0 - x1;
+                    }
+#pragma unroll
+        for (int m = 1; m < L; m <<= 1) {
+            const float sgn = (i0 & m) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int g = 0; g < P; ++g)
+#pragma unroll
+                for (int j = 0; j < E; ++j) e[g][j] = fmaf(sgn, e[g][j], __shfl_xor_sync(kFull, e[g][j], m));
+        }
+#pragma unroll
+        for (int g = 0; g < P; ++g)
+            if (on[g]) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) base[g][L * j * 33] = e[g][j];
+            }
+    }
+}
+
+TQ_DEVFN void hadamard_columns(float* xf, int nrows, int M, int warp, int nwarps, int lane) {
+    switch (M) {
+        case 1: break;
+        case 2: hadamard_columns_m<2>(xf, nrows, warp, nwarps, lane); break;
+        case 4: hadamard_columns_m<4>(xf, nrows, warp, nwarps, lane); break;
+        case 8: hadamard_columns_m<8>(xf, nrows, warp, nwarps, lane); break;
+        case 16: hadamard_columns_m<16>(xf, nrows, warp, nwarps, lane); break;
+        case 32: hadamard_columns_m<32>(xf, nrows, warp, nwarps, lane); break;
+        case 64: hadamard_columns_m<64>(xf, nrows, warp, nwarps, lane); break;
+        case 128: hadamard_columns_m<128>(xf, nrows, warp, nwarps, lane); break;
+        default: hadamard_columns_m<256>(xf, nrows, warp, nwarps, lane); break;
+    }
+}
+
 struct TritMaps {
     CUtensorMap codes;   // [experts][rows][row_stride] words, box 32 x 16 x 1, 128-byte swizzle
     CUtensorMap scales;  // [experts][rows][ngroups] fp16, box 40 x 16 x 1
@@ -824,7 +896,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
     uint64_t* empty = full + kTcSlots;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTcSlots);
     int* tag = reinterpret_cast<int*>(empty + kTcSlots + 1);            // [slots]: (task << 8) | stage, or -1
-    float* rowsum = reinterpret_cast<float*>(tag + (kTcSlots + 3) / 4 * 4);  // [tasks of this CTA][RT]
+    float* xf = reinterpret_cast<float*>(tag + (kTcSlots + 3) / 4 * 4);  // [cols / 32][33] input stage (xmode != 0)
+    float* rowsum = xf + (tp.xmode ? (p.cols / 32) * 33 : 0);             // [tasks of this CTA][RT]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
@@ -924,9 +997,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
 
     // ---------------- consumers
     const int cw = warp - 1, ctid = tid - 32;
+    // input stage: quads of 4 columns of vector vec, 4 per thread in flight (r = 0..3 -> quad ctid + r NCT)
+    const int nq = p.cols / 4;
+    auto load_quads = [&](int64_t vec, int q0, float4 (&xv4)[4], uint32_t (&sg)[4]) {
+        const uint32_t* sg4 = reinterpret_cast<const uint32_t*>(tp.xsigns);  // 4 signs per word
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int q = q0 + ctid + r * NCT;
+            if (q < nq) {
+                sg[r] = __ldg(sg4 + q);
+                if (tp.xmode == 1) {
+                    if (tp.xdt == TQ_F32) {
+                        xv4[r] = __ldg(reinterpret_cast<const float4*>(tp.xin) + vec * nq + q);
+                    } else {
+                        const uint2 b = __ldg(reinterpret_cast<const uint2*>(tp.xin) + vec * nq + q);
+                        xv4[r] = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u),
+                                             __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u));
+                    }
+                } else {
+                    const float4* gu = reinterpret_cast<const float4*>(tp.xin) + vec * 2 * nq;
+                    const float4 g = __ldg(gu + q), u = __ldg(gu + nq + q);
+                    xv4[r] = make_float4(g.x / (1.0f + expf(-g.x)) * u.x, g.y / (1.0f + expf(-g.y)) * u.y,
+                                         g.z / (1.0f + expf(-g.z)) * u.z, g.w / (1.0f + expf(-g.w)) * u.w);
+                }
+            }
+        }
+    };
+    float4 pre_x[4];
+    uint32_t pre_sg[4];
+    const int64_t pre_vec = tp.xmode != 0 && t_begin < t_end && nq <= 4 * NCT ? vec_of(t_begin / tpi) : -1;
+    if (pre_vec >= 0) load_quads(pre_vec, 0, pre_x, pre_sg);  // in flight while the table is built
     if (t_begin < t_end) {  // start fetching the first input vector while the table is built
-        const char* x0 = reinterpret_cast<const char*>(p.x + (int64_t)vec_of(t_begin / tpi) * p.cols);
-        for (int off = ctid * 128; off < p.cols * 4; off += NCT * 128)
+        const int64_t v0 = vec_of(t_begin / tpi);
+        const int64_t bytes = tp.xmode == 0 ? (int64_t)p.cols * 4
+                              : tp.xmode == 1 ? (int64_t)p.cols * (tp.xdt == TQ_F32 ? 4 : 2)
+                                              : (int64_t)p.cols * 8;  // [gate | up] in f32
+        const char* x0 = tp.xmode == 0 ? reinterpret_cast<const char*>(p.x) : reinterpret_cast<const char*>(tp.xin);
+        x0 += v0 * bytes;
+        for (int64_t off = ctid * 128; off < bytes; off += NCT * 128)
             asm volatile("prefetch.global.L1 [%0];" ::"l"(x0 + off));
     }
     for (int i = ctid; i < 81 * 32; i += NCT) {
@@ -968,7 +1076,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             auto pack = [](int qlo, int qhi) { return ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16); };
             constexpr int kV4 = 4;  // 16-byte input loads per thread when the vector fits
             const int nv4 = p.cols >> 2;
-            if ((p.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(xv) & 15) == 0 && nv4 <= kV4 * NCT) {
+            if (tp.xmode != 0) {
+                // The input stage: x (or silu(gate) * up) times the signs, into rows of 32 floats
+                // padded to 33, then the block Hadamard transform of the rotation as 32-point
+                // transforms along the rows and M-point transforms down the columns of every
+                // block (H_{32M} = H_M (x) H_32), scaled by 1 / sqrt(block) through yscale.
+                const int K = p.cols, nrows = K / 32;
+                // quads of 4 columns, 4 quads per thread in flight at a time
+                for (int q0 = 0; q0 < nq; q0 += 4 * NCT) {
+                    float4 xv4[4];
+                    uint32_t sg[4];
+                    if (q0 == 0 && vec == pre_vec) {  // loaded at the start
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            xv4[r] = pre_x[r];
+                            sg[r] = pre_sg[r];
+                        }
+                    } else {
+                        load_quads(vec, q0, xv4, sg);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int q = q0 + ctid + r * NCT;
+                        if (q < nq) {
+                            const int k = 4 * q;  // 4 columns inside one row of 32
+                            float* dst = xf + (k >> 5) * 33 + (k & 31);
+                            dst[0] = xv4[r].x * (float)(int8_t)(sg[r]);
+                            dst[1] = xv4[r].y * (float)(int8_t)(sg[r] >> 8);
+                            dst[2] = xv4[r].z * (float)(int8_t)(sg[r] >> 16);
+                            dst[3] = xv4[r].w * (float)(int8_t)(sg[r] >> 24);
+                        }
+                    }
+                }
+                named_bar_sync(1, NCT);
+                for (int r0 = cw; r0 < nrows; r0 += 4 * NC) {  // four independent rows per pass
+                    float v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = r0 + i * NC < nrows ? xf[(r0 + i * NC) * 33 + lane] : 0.f;
+#pragma unroll
+                    for (int m = 1; m < 32; m <<= 1) {
+                        const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] = fmaf(sgn, v[i], __shfl_xor_sync(kFull, v[i], m));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (r0 + i * NC < nrows) xf[(r0 + i * NC) * 33 + lane] = v[i];
+                }
+                named_bar_sync(1, NCT);
+                hadamard_columns(xf, nrows, tp.xblock / 32, cw, NC, lane);
+                named_bar_sync(1, NCT);
+                float mx = 0.f;
+                for (int k = ctid; k < K; k += NCT) mx = fmaxf(mx, fabsf(xf[(k >> 5) * 33 + (k & 31)]));
+#pragma unroll
+                for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+                if (lane == 0) red[cw] = mx;
+                named_bar_sync(1, NCT);
+                mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) mx = fmaxf(mx, red[i]);
+                const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+                const float rs = rsqrtf((float)tp.xblock);
+                yscale = delta * (rs * mx / 32767.0f);
+                for (int k = 2 * ctid; k < nunits_pad * F::kUT; k += 2 * NCT) {
+                    const float lo = k < K ? xf[(k >> 5) * 33 + (k & 31)] : 0.f;
+                    const float hi = k + 1 < K ? xf[((k + 1) >> 5) * 33 + ((k + 1) & 31)] : 0.f;
+                    xb[pair_at(k)] = pack(__float2int_rn(lo * inv), __float2int_rn(hi * inv));
+                }
+                if (has_off) {
+                    for (int g = ctid; g < nunits_pad * GPU; g += NCT) {
+                        float sum = 0.f;
+                        for (int k = g * G; k < min((g + 1) * G, K); ++k) sum += xf[(k >> 5) * 33 + (k & 31)];
+                        xsum[g] = rs * sum;
+                    }
+                }
+            } else if ((p.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(xv) & 15) == 0 && nv4 <= kV4 * NCT) {
                 float4 xr[kV4];
                 float mx = 0.f;
 #pragma unroll
@@ -1012,7 +1194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
                     xb[pair_at(k)] = pack(__float2int_rn(lo * inv), __float2int_rn(hi * inv));
                 }
             }
-            if (has_off) {
+            if (has_off && tp.xmode == 0) {
                 for (int g = ctid; g < nunits_pad * GPU; g += NCT) {
                     float sum = 0.f;
                     for (int k = g * G; k < min((g + 1) * G, p.cols); ++k) sum += __ldg(xv + k);
@@ -1111,11 +1293,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
     __syncthreads();  // the producer drains its copies on an abort before the CTA exits
 }
 
-size_t trit_tc_smem(int nsteps, int max_tasks) {
+size_t trit_tc_smem(int nsteps, int max_tasks, int xf_floats) {
     const size_t nunits_pad = (size_t)nsteps * kTcS;
     return 1024 + (size_t)kTcSlots * (kTcCode + kTcScale) + 4 * ((size_t)81 * 32 + 32) + 4 * nunits_pad * kTcUS +
            4 * ((nunits_pad * 5 + 3) / 4 * 4) + 8 * (size_t)(2 * kTcSlots + 1) + 4 * (size_t)((kTcSlots + 3) / 4 * 4) +
-           4 * (size_t)max_tasks * kTcRows;
+           4 * (size_t)xf_floats + 4 * (size_t)max_tasks * kTcRows;
 }
 
 // Tensor maps of the code and scale banks (3-D: experts x rows x row).
@@ -1158,9 +1340,10 @@ bool trit_tc_ok(const QmvParams& qp, int group) {
            tensor_map_encoder() != nullptr;
 }
 
-tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st) {
+tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st, const TritParams* xstage) {
     using F = TritFmt<16>;
     TritParams tp{};
+    if (xstage) tp = *xstage;
     tp.q = qp;
     tp.units = (qp.cols + F::kUT - 1) / F::kUT;
     tp.nsteps = (tp.units + kTcS - 1) / kTcS;
@@ -1182,7 +1365,7 @@ tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st) {
     if (grid < 1) grid = 1;
     if (grid > 0x7fffffffll) return TQ_ERR_UNSUPPORTED;
     const int max_tasks = (int)((total + grid - 1) / grid) + 1;
-    const size_t smem = trit_tc_smem(tp.nsteps, max_tasks);
+    const size_t smem = trit_tc_smem(tp.nsteps, max_tasks, tp.xmode ? (qp.cols / 32) * 33 : 0);
     if (smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
     TritMaps maps;
     if (!encode_trit_maps(qp, maps)) return TQ_ERR_UNSUPPORTED;
@@ -1193,6 +1376,23 @@ tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st) {
 }
 
 }  // namespace
+
+// The tensor-copy kernel with its input stage (xmode 1: rotate xin rows; 2: SwiGLU then rotate).
+tq_status qmv_trit_xstage_run(const QmvParams& p, int group, int n_items, int xmode, const void* xin, int xdt,
+                              const int8_t* signs, int block, cudaStream_t st) {
+    // 16-byte input loads (8-byte for bf16) and one 32-bit word per 4 signs
+    const uintptr_t xa = xmode == 1 && xdt == TQ_BF16 ? 7 : 15;
+    if (!trit_tc_ok(p, group) || p.cols % 32 || block < 32 || block > 8192 || (block & (block - 1)) ||
+        p.cols % block || (reinterpret_cast<uintptr_t>(xin) & xa) || (reinterpret_cast<uintptr_t>(signs) & 3))
+        return TQ_ERR_UNSUPPORTED;
+    TritParams xs{};
+    xs.xmode = xmode;
+    xs.xin = xin;
+    xs.xdt = xdt;
+    xs.xsigns = signs;
+    xs.xblock = block;
+    return launch_trit_tc(p, n_items, st, &xs);
+}
 
 // Rows per warp step: 4 rows x 8 units when a row holds many units, else 8 rows
 // x 4 units (keeps the last, partial step of short rows cheap).
@@ -1205,7 +1405,7 @@ tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t 
     if (pipe_ok) {
         // group 16: the tensor-copy pipeline when the banks can be described by tensor maps
         if (trit_tc_ok(p, group)) {
-            const tq_status s = launch_trit_tc(p, n_items, st);
+            const tq_status s = launch_trit_tc(p, n_items, st, nullptr);
             if (s != TQ_ERR_UNSUPPORTED) return s;
         }
         return group == 16 ? launch_trit_pipe<16>(p, n_items, st) : launch_trit_pipe<32>(p, n_items, st);

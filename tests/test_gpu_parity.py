@@ -309,6 +309,46 @@ def test_moe_decode_layer(lib):
     assert rel_l2(out, ref) < REL_L2
 
 
+@pytest.mark.parametrize("E,k,H,I", [(16, 4, 1024, 512), (4, 2, 2048, 256)])
+def test_moe_decode_fused_stages(lib, E, k, H, I):
+    """The decode layer with the input rotation inside gate/up and SwiGLU + rotation inside down:
+    against the oracle, and the gate/up outputs against the separate rotate + gather_qmv calls."""
+    seed = wl.SEED_MOE_DECODE + 7
+    logits = wl.router_logits(seed, 1, E)
+    xb, x = wl.activations(seed, 1, H)
+    gu_bank = [wl.expert_weights(seed, e, 0, 2 * I, H)[1] for e in range(E)]
+    dn_bank = [wl.expert_weights(seed, e, 1, H, I)[1] for e in range(E)]
+    sH, sI = o.rotation_signs(wl.sign_seed(seed, 0), H), o.rotation_signs(wl.sign_seed(seed, 1), I)
+    bH, bI = o.rotation_block(H), o.rotation_block(I)
+    ct, tt = o.lloyd_max_gaussian(3)
+    rotH, rotI = lib.Rotation(H, bH, signs=sH), lib.Rotation(I, bI, signs=sI)
+    cb = lib.Codebook(3)
+    gu_codes, gu_scales = lib.quantize(_dev(np.concatenate(gu_bank)), 16, rotH, cb)
+    dn_codes, dn_scales = lib.quantize(_dev(np.concatenate(dn_bank)), 16, rotI, cb)
+    qgu = lib.QWeight(gu_codes, gu_scales, E, 2 * I, H, 16, cb)
+    qdn = lib.QWeight(dn_codes, dn_scales, E, H, I, 16, cb)
+    ids, probs, _, _, _ = lib.moe_route(_dev(logits), k)
+    gu_f = lib.gather_qmv_rotate(qgu, _dev(x), rotH, ids)
+    gu_s = lib.gather_qmv(qgu, lib.rotate(_dev(x), rotH), ids)
+    assert rel_l2(gu_f.cpu().numpy(), gu_s.cpu().numpy()) < 1e-4
+    gu_b = lib.gather_qmv_rotate(qgu, _bf16_dev(xb), rotH, ids)  # bf16 input, the same values
+    assert rel_l2(gu_b.cpu().numpy(), gu_f.cpu().numpy()) < 1e-6
+    yd = lib.multi_gather_qmv_swiglu(qdn, gu_f.reshape(k, 2 * I), rotI, ids.reshape(-1))
+    out = lib.moe_combine(yd, probs, k).cpu().numpy()
+    oids, oprobs = o.route(logits, k)
+    RH, RI = o.rotation_matrix(sH, bH), o.rotation_matrix(sI, bI)
+
+    def bank(ws, R, e):
+        c, s16 = o.encode_rotated(ws[e].astype(np.float64) @ R.T, 16, tt)
+        return o.dequantize(c, s16, ct, 16)
+
+    gu_o = o.gather_qmv(lambda e: bank(gu_bank, RH, e), oids, o.rotate(x, sH, bH))
+    h_o = o.rotate(o.swiglu(gu_o.reshape(k, 2 * I), I), sI, bI)
+    yd_o = o.multi_gather_qmv(lambda e: bank(dn_bank, RI, e), oids.reshape(-1), h_o)
+    ref = o.combine(yd_o.reshape(1, k, H), oprobs)
+    assert rel_l2(out, ref) < REL_L2
+
+
 @pytest.mark.parametrize("T,klev,vlev,group", [(300, 256, 8, 32), (2100, 256, 8, 32), (65, 16, 16, 16)])
 def test_kv_quantize_and_attend(lib, T, klev, vlev, group):
     Hkv, D, Hq = 8, 128, 32
