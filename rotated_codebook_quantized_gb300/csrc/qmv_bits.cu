@@ -148,14 +148,16 @@ __global__ void __launch_bounds__(256, 2) qmv_bits_kernel(const BitsParams bp) {
         }
         __syncthreads();  // previous segment's row sums written out, x no longer read
 
-        // This warp's share: a contiguous range of (task, chunk stage) pairs, each SUB part stages.
-        const int ncs_seg = (s1 - s0) * nsc;
-        const int f_begin = (int)((int64_t)warp * ncs_seg / nwarps);
-        const int f_end = (int)((int64_t)(warp + 1) * ncs_seg / nwarps);
-        const int L = (f_end - f_begin) * SUB;  // part stages
+        // This warp's share: a contiguous range of part stages (SUB per chunk stage, nsc chunk
+        // stages per task); a share may start or end inside a chunk stage.
+        const int nps = nsc * SUB;  // part stages per task
+        const int nparts_seg = (s1 - s0) * nps;
+        const int f_begin = (int)((int64_t)warp * nparts_seg / nwarps);
+        const int f_end = (int)((int64_t)(warp + 1) * nparts_seg / nwarps);
+        const int L = f_end - f_begin;  // part stages
 
-        // producer: task pt, chunk stage pcs, part pp; pword: word of this lane's first piece
-        int pt = s0 + f_begin / nsc, pcs = f_begin % nsc, pp = 0, pslot = 0;
+        // producer: task pt, chunk stage pcs, part pp
+        int pt = s0 + f_begin / nps, pcs = (f_begin % nps) / SUB, pp = f_begin % SUB, pslot = 0;
         const uint32_t* pcode = nullptr;
         const uint16_t* pscale = nullptr;
         auto set_prod_task = [&]() {
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(256, 2) qmv_bits_kernel(const BitsParams bp) {
         }
         __syncthreads();
 
-        int ct = s0 + f_begin / nsc, ccs = f_begin % nsc, cpart = 0, cslot = 0;
+        int ct = s0 + f_begin / nps, ccs = (f_begin % nps) / SUB, cpart = f_begin % SUB, cslot = 0;
         bool cbad;
         {
             int e, v;
@@ -245,6 +247,8 @@ __global__ void __launch_bounds__(256, 2) qmv_bits_kernel(const BitsParams bp) {
         }
         float tot = 0.f;
         float acc[GPC];
+#pragma unroll
+        for (int g = 0; g < GPC; ++g) acc[g] = 0.f;  // a share may start inside a chunk stage
         for (int j = 0; j < L; ++j) {
             cp_wait<NS - 2>();  // stage j has landed
             __syncwarp();       // and every lane is done with the slot of stage j - 1
@@ -320,30 +324,35 @@ __global__ void __launch_bounds__(256, 2) qmv_bits_kernel(const BitsParams bp) {
                     if (cpart == decltype(pc)::value) decode_part(pc);
                 });
             }
-            if (cpart == SUB - 1) {
+            const bool last = j == L - 1;
+            if (cpart == SUB - 1 || last) {  // the chunk stage's (or this share's) group sums, scaled
                 const uint16_t* ssrc =
                     reinterpret_cast<const uint16_t*>(stg + RPW * B::kCodeRow + r * B::kScaleRow) + c * GPC;
 #pragma unroll
                 for (int g = 0; g < GPC; ++g) tot = fmaf(half_bits_to_float(ssrc[g]), acc[g], tot);
             }
             cslot = cslot + 1 == NS ? 0 : cslot + 1;
-            if (++cpart < SUB) continue;
-            cpart = 0;
-            if (++ccs == nsc || j == L - 1) {  // task finished or this warp's share ends: add the row sums
+            const bool stage_end = ++cpart == SUB;
+            if (stage_end) {
+                cpart = 0;
+                ++ccs;
+            }
+            const bool task_end = stage_end && ccs == nsc;
+            if (task_end || last) {  // task finished or this warp's share ends: add the row sums
                 float v = cbad ? 0.f : tot;
 #pragma unroll
                 for (int m = 1; m < UPW; m <<= 1) v += __shfl_xor_sync(kFull, v, m);
                 if (c == 0) atomicAdd(rowsum + (ct - s0) * RPW + r, v);
                 tot = 0.f;
-                if (ccs == nsc) {
-                    ccs = 0;
-                    ++ct;
-                    if (ct < s1) {
-                        int e, vv;
-                        item_info(ct / tpi, e, vv);
-                        cbad = e < 0 || e >= p.experts;
-                        if (cbad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
-                    }
+            }
+            if (task_end) {
+                ccs = 0;
+                ++ct;
+                if (ct < s1) {
+                    int e, vv;
+                    item_info(ct / tpi, e, vv);
+                    cbad = e < 0 || e >= p.experts;
+                    if (cbad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
                 }
             }
         }
