@@ -263,6 +263,26 @@ tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtype xdt, cons
                         void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
 size_t tq_gather_qmm_workspace_bytes(int32_t P, int32_t cols, int32_t per_pair_input);
 
+/* Dense matvec on the tensor cores: y[t, :] = W x_rot[t] for expert 0 of w, as
+ * tq_qmv computes it, with fp16 operands.
+ * "How it works", "Running a quantized layer" (the rotated input times the
+ * codes, decoded inline; the full-precision weights are never written out).
+ * Each input row is scaled by the power of two 2^e_t just above its largest
+ * magnitude and rounded to fp16; the decoded weights c[code] * s_group are
+ * formed in fp16; products accumulate in fp32 and the outputs are scaled back
+ * by 2^e_t.  The columns are split among the SMs and
+ * the partial sums added with atomics (the summation order varies from run to
+ * run).  x_rot: device f32 [T, cols].  y: device f32 [T, rows] (overwritten).
+ * ws: 16-byte aligned device scratch of at least tq_qmv_tc_workspace_bytes(T,
+ * cols) bytes (TQ_ERR_INVALID if smaller); it holds the fp16 rows and their
+ * scales and must not be shared with a call running concurrently.
+ * TQ_ERR_UNSUPPORTED (nothing launched) unless cb->levels is 4, 8 or 16, rows
+ * is a multiple of 128, cols a multiple of 64 with at most 64 groups per row,
+ * and 1 <= T <= 64; tq_qmv covers the other cases. */
+tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_t T, float* y, void* ws, size_t ws_bytes,
+                    void* stream);
+size_t tq_qmv_tc_workspace_bytes(int32_t T, int32_t cols);
+
 /* Dequantize selected experts to dense rotated-domain weights, for a regular matmul.
  * "How it works", row "Anything else" (polar_dequant_experts).
  * out[i, n, c] = fp16 scale * centroid of expert ids[i]; out: device

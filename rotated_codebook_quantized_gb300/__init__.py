@@ -54,6 +54,8 @@ _SIGS = {
     "tq_quantize": (_i32, [_c_p, _i32, _i64, _i32, _i32, _P(tq_rotation_t), _P(tq_codebook_t), _c_p, _c_p, _i64,
                            _c_p]),
     "tq_qmv": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p]),
+    "tq_qmv_tc": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _sz, _c_p]),
+    "tq_qmv_tc_workspace_bytes": (_sz, [_i32, _i32]),
     "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p]),
     "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
     "tq_gather_qmv_rotate": (_i32, [_P(tq_qweight_t), _c_p, _i32, _P(tq_rotation_t), _c_p, _i32, _i32, _c_p, _i32,
@@ -247,13 +249,36 @@ def quantize(W, group: int, rot: Rotation, cb: Codebook, row_stride: int | None 
     return codes, scales
 
 
-def qmv(w: QWeight, x_rot, out_dtype=None):
+def qmv(w: QWeight, x_rot, out_dtype=None, tensor_cores=True):
+    """y = W x_rot for every row of x_rot.  With tensor_cores, an f32 output and two or more
+    rows, the tq_qmv_tc form runs where it applies (fp16 operands, fp32 sums; at one row the
+    CUDA-core kernel is as fast); elsewhere tq_qmv."""
     torch = _torch()
     _contig(x_rot, "x_rot")
     T = x_rot.shape[0]
     y = torch.empty((T, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
     q = w.c()
+    if tensor_cores and y.dtype == torch.float32 and T >= 2:
+        nb = int(load().tq_qmv_tc_workspace_bytes(T, w.cols))
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=x_rot.device)
+        st = load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, _stream())
+        if st != TQ_ERR_UNSUPPORTED:
+            _check(st, "tq_qmv_tc")
+            return y
     _check(load().tq_qmv(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _dt(y), _stream()), "tq_qmv")
+    return y
+
+
+def qmv_tc(w: QWeight, x_rot):
+    """The tensor-core dense matvec alone (raises TQError where it does not apply)."""
+    torch = _torch()
+    _contig(x_rot, "x_rot")
+    T = x_rot.shape[0]
+    y = torch.empty((T, w.rows), dtype=torch.float32, device=x_rot.device)
+    nb = int(load().tq_qmv_tc_workspace_bytes(T, w.cols))
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=x_rot.device)
+    q = w.c()
+    _check(load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, _stream()), "tq_qmv_tc")
     return y
 
 

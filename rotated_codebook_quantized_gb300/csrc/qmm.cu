@@ -21,6 +21,7 @@
 // running together share the expert's codes in L2.  Every wait on an mbarrier
 // is bounded; on expiry the CTA sets TQ_DEVERR_TIMEOUT, drains and frees TMEM.
 
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -153,6 +154,7 @@ struct QmmParams {
     void* y;
     int ydt;
     uint32_t* err;
+    const float* colscale;  // per pair row of x: factor applied to its outputs (may be null)
 };
 
 template <int LEVELS, int G, int XT>
@@ -516,9 +518,14 @@ constexpr int pow2_at_least(int v) {
     return p;
 }
 
-template <int LEVELS, int G>
+template <int LEVELS, int G, int NT, int ST>
 struct Q2Fmt {
     using F = BitFmt<LEVELS>;
+    static_assert(NT == 256 || (NT >= 16 && NT <= 128 && NT % 16 == 0), "pair tile");
+    static constexpr int kBBytes = NT * kBK * 2;                // one B stage
+    static constexpr int kHalf = NT <= 128 ? NT : 128;          // columns of one MMA thread's accumulator
+    static constexpr int kBuf = 2 * kHalf;                      // columns of one accumulator buffer
+    static constexpr int kTmemCols = 2 * kBuf;                  // two buffers
     static constexpr int kSPC = F::kCW / 2;                    // stages (64 codes) per 32-word chunk
     static constexpr int kCPC = 32 * F::kCW;                   // codes per chunk
     static constexpr int kLutCopies = LEVELS == 16 ? 1 : 32;  // per-lane copies when small enough
@@ -527,8 +534,9 @@ struct Q2Fmt {
     static constexpr int kChunkBytes = kChunkCodeBytes + kBM * kSW * 4;
     // A and B stages share one ring (one full and one empty barrier per stage, so the MMA
     // thread waits once and commits once per stage).
-    static constexpr int kStages = 3;
-    static constexpr int kSmem = 1024 + kStages * (kABytes + kBBytes) + kChunkSlots * kChunkBytes + kLutBytes + 64 * 8 +
+    static constexpr int kStages = ST;
+    static_assert(2 * ST + 2 * kChunkSlots + 5 <= 64, "barrier area");
+    static constexpr int kSmem = 8192 + kStages * (kABytes + kBBytes) + kChunkSlots * kChunkBytes + kLutBytes + 64 * 8 +
                                  32;  // plus 8 * (experts + 1)
     static_assert(kSW <= 16, "scale words per chunk row");
 };
@@ -577,20 +585,29 @@ TQ_DEVFN void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
 TQ_DEVFN void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
-template <int LEVELS, int G, int XT>
+// SK (split K, one expert, all pairs in one tile of at most NT): the work is the
+// (row tile, code chunk) units, and CTA b takes a contiguous range of them, so
+// every SM has work even when the row tiles are fewer than the SMs; each run of
+// a row tile's chunks is one item, whose partial sums are added to y (zeroed
+// beforehand) with atomics.
+template <int LEVELS, int G, int XT, int NT, int ST, bool SK>
 __global__ void __launch_bounds__(kThreads2, 1)
     gather_qmm2_kernel(const QmmParams p, const __grid_constant__ QmmMaps tm) {
     using F = BitFmt<LEVELS>;
-    using Q = Q2Fmt<LEVELS, G>;
+    using Q = Q2Fmt<LEVELS, G, NT, ST>;
     constexpr int SPC = Q::kSPC, CPC = Q::kCPC, NL = LEVELS * LEVELS, COPIES = Q::kLutCopies;
-    constexpr int kStages = Q::kStages, kChunkBytes = Q::kChunkBytes, SW = Q::kSW;
+    constexpr int kStages = Q::kStages, kChunkBytes = Q::kChunkBytes, SW = Q::kSW, kBBytes = Q::kBBytes;
+    constexpr int kHalf = Q::kHalf, kBuf = Q::kBuf;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = base;                                      // [kStages][128 x 64]
-    uint8_t* sB = sA + kStages * kABytes;                    // [kStages][256 x 64]
-    uint8_t* sC = sB + kStages * kBBytes;                    // [2] x (codes 128 x 128 B, scales 128 x SW words)
-    uint32_t* lut = reinterpret_cast<uint32_t*>(sC + kChunkSlots * kChunkBytes);  // [NL][COPIES] operand pairs
-    uint64_t* bars = reinterpret_cast<uint64_t*>(lut + NL * COPIES);
+    // The table sits at an 8 KB boundary, so its per-lane entry addresses are ORs of disjoint bit
+    // fields (lane * 4 in bits 2..6, the code pair above); the tiles follow at 1 KB multiples.
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 8191) & ~uintptr_t(8191));
+    uint32_t* lut = reinterpret_cast<uint32_t*>(base);                    // [NL][COPIES] operand pairs
+    uint8_t* sA = base + Q::kLutBytes;                                    // [kStages][128 x 64]
+    uint8_t* sB = sA + kStages * kABytes;                                 // [kStages][NT x 64]
+    uint8_t* sC = sB + kStages * kBBytes;  // [2] x (codes 128 x 128 B, scales 128 x SW words)
+    static_assert(Q::kLutBytes % 1024 == 0, "table size");
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kChunkSlots * kChunkBytes);
     // full[s]: stage s's A (its decoder group) and B (the copy's bytes) are in place;
     // empty[s]: the MMAs that read stage s have completed.
     uint64_t* full = bars;
@@ -614,28 +631,33 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int ngroups = p.cols / G;
     const int nchunks = (nk + SPC - 1) / SPC;
 
-    for (int i = tid; i <= E; i += kThreads2) cum[i] = offs[i] = p.offsets[i];
+    if constexpr (!SK)
+        for (int i = tid; i <= E; i += kThreads2) cum[i] = offs[i] = p.offsets[i];
     for (int i = tid; i < NL * COPIES; i += kThreads2) {
         const int idx = i / COPIES;
         lut[i] = pack2<XT>(p.centroids[idx & (LEVELS - 1)], p.centroids[idx / LEVELS]);
     }
     __syncthreads();
     if (tid == 0) {
-        bool ok = cum[0] == 0 && cum[E] == p.P;
-        int prev = 0, acc = 0;
-        for (int e = 0; e <= E; ++e) {
-            const int off = cum[e];
-            if (e > 0) {
-                const int n = off - prev;
-                ok = ok && n >= 0;
-                const int nt = n > 0 ? (n + kNT - 1) / kNT : 0;
-                cum[e - 1] = acc;
-                acc += nt * mtiles;
+        if constexpr (SK) {
+            *total_items = mtiles * nchunks;  // units
+        } else {
+            bool ok = cum[0] == 0 && cum[E] == p.P;
+            int prev = 0, acc = 0;
+            for (int e = 0; e <= E; ++e) {
+                const int off = cum[e];
+                if (e > 0) {
+                    const int n = off - prev;
+                    ok = ok && n >= 0;
+                    const int nt = n > 0 ? (n + NT - 1) / NT : 0;
+                    cum[e - 1] = acc;
+                    acc += nt * mtiles;
+                }
+                prev = off;
             }
-            prev = off;
+            cum[E] = acc;
+            *total_items = ok ? acc : -1;
         }
-        cum[E] = acc;
-        *total_items = ok ? acc : -1;
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 32 * kDec2 / 2 + 1);  // a decoder group + the B copy
@@ -660,7 +682,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(2 * kNT)
+                     "r"(Q::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -669,20 +691,54 @@ __global__ void __launch_bounds__(kThreads2, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto item_coords = [&](int item, int& e, int& mt, int& nt, int& i0, int& nvalid) {
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (cum[mid] <= item) lo = mid; else hi = mid - 1;
+    // One item: chunks [c0, c1) (stages [kb, ke)) of row tile mt of expert e against pair
+    // tile nt (pairs i0 .. i0 + nvalid - 1).  Every role walks the same item sequence.
+    struct Item {
+        int e, mt, nt, i0, nvalid, c0, c1, kb, ke, state;
+    };
+    const int ub = SK ? (int)((int64_t)blockIdx.x * total / gridDim.x) : 0;  // this CTA's units (SK)
+    const int ue = SK ? (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x) : 0;
+    auto load_item = [&](Item& I) -> bool {
+        if constexpr (SK) {
+            const int u = I.state;
+            if (u >= ue) return false;
+            I.e = 0;
+            I.nt = 0;
+            I.i0 = 0;
+            I.nvalid = p.P;
+            I.mt = u / nchunks;
+            I.c0 = u - I.mt * nchunks;
+            I.c1 = min(nchunks, I.c0 + (ue - u));
+        } else {
+            const int item = I.state;
+            if (item >= total) return false;
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (cum[mid] <= item) lo = mid; else hi = mid - 1;
+            }
+            I.e = lo;
+            const int off0 = offs[lo], n = offs[lo + 1] - off0;
+            const int ntiles = (n + NT - 1) / NT;
+            const int local = item - cum[lo];
+            I.mt = local / ntiles;
+            I.nt = local - I.mt * ntiles;
+            I.i0 = off0 + I.nt * NT;
+            I.nvalid = min(NT, n - I.nt * NT);
+            I.c0 = 0;
+            I.c1 = nchunks;
         }
-        e = lo;
-        const int off0 = offs[e], n = offs[e + 1] - off0;
-        const int ntiles = (n + kNT - 1) / kNT;
-        const int local = item - cum[e];
-        mt = local / ntiles;
-        nt = local - mt * ntiles;
-        i0 = off0 + nt * kNT;
-        nvalid = min(kNT, n - nt * kNT);
+        I.kb = I.c0 * SPC;
+        I.ke = min(I.c1 * SPC, nk);
+        return true;
+    };
+    auto first_item = [&](Item& I) -> bool {
+        I.state = SK ? ub : (int)blockIdx.x;
+        return load_item(I);
+    };
+    auto next_item = [&](Item& I) -> bool {
+        I.state += SK ? I.c1 - I.c0 : (int)gridDim.x;
+        return load_item(I);
     };
 
     if (warp < kMmaWarps) {
@@ -697,27 +753,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
             uint32_t it = 0, tile_it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++tile_it) {
-                int e, mt, nt, i0, nvalid;
-                item_coords(item, e, mt, nt, i0, nvalid);
-                const int ninst = (nvalid + 15) & ~15;
-                const bool ksplit = ninst <= 128 && nk >= 2;
+            Item I;
+            for (bool have = first_item(I); have && ok; have = next_item(I), ++tile_it) {
+                const int kb = I.kb, ke = I.ke;
+                const int ninst = (I.nvalid + 15) & ~15;
+                const bool ksplit = ninst <= 128 && ke - kb >= 2;
                 const int ncols = ksplit ? ninst : (me == 0 ? min(ninst, 128) : ninst - 128);
                 const uint32_t idesc = f16_idesc(XT, ncols > 0 ? ncols : 16);
                 const int buf = tile_it & 1;
                 if (!mbar_wait(tile_empty + buf, ((tile_it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * kNT + me * 128);
+                const uint32_t d = tmem + (uint32_t)(buf * kBuf + me * kHalf);
                 const uint32_t boff = ksplit ? 0u : (uint32_t)(me * 128 * 128);  // B rows of thread 1's columns
-                for (int kc = 0; kc < nk; ++kc, ++it) {
+                for (int kc = kb; kc < ke; ++kc, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const bool mine = ksplit ? (kc & 1) == me : ncols > 0;
+                    const bool mine = ksplit ? ((kc - kb) & 1) == me : ncols > 0;
                     if (mine) {
-                        const bool first = ksplit ? kc == me : kc == 0;
+                        const bool first = ksplit ? kc - kb == me : kc == kb;
                         const uint64_t ad = sw128_desc(a0 + s * kABytes), bd = sw128_desc(b0 + s * kBBytes + boff);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -735,17 +791,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
     } else if (warp < kMmaWarps + kBWarps) {
         // ------------------------------------------------ B: one tensor copy per stage, warps alternate stages
         if (lane == 0) {
+            if constexpr (SK) asm volatile("griddepcontrol.wait;" ::: "memory");  // x16 written
             const int bw = warp - kMmaWarps;
             const uint32_t b0 = smem_u32(sB);
             uint32_t it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                int e, mt, nt, i0, nvalid;
-                item_coords(item, e, mt, nt, i0, nvalid);
+            Item I;
+            for (bool have = first_item(I); have && ok; have = next_item(I)) {
                 int bi = 0;
-                while (bi < 4 && (128 >> bi) >= nvalid) ++bi;  // smallest box of 256 >> bi rows >= nvalid
-                const int box_rows = 256 >> bi;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
+                while (bi < 4 && (128 >> bi) >= I.nvalid) ++bi;  // smallest box of 256 >> bi rows >= nvalid
+                const int box_rows = 256 >> bi;                   // at most NT (the host checks)
+                const int i0 = I.i0;
+                for (int kc = I.kb; kc < I.ke; ++kc, ++it) {
                     if ((int)(it % kBWarps) != bw) continue;
                     const int s = it % kStages;
                     if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -767,10 +824,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const uint32_t c0 = smem_u32(sC);
             uint32_t cc = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                int e, mt, nt, i0, nvalid;
-                item_coords(item, e, mt, nt, i0, nvalid);
-                for (int c = 0; c < nchunks; ++c, ++cc) {
+            Item I;
+            for (bool have = first_item(I); have && ok; have = next_item(I)) {
+                const int e = I.e, mt = I.mt;
+                for (int c = I.c0; c < I.c1; ++c, ++cc) {
                     const int slot = cc % kChunkSlots;
                     if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(cfull + slot, (uint32_t)kChunkCodeBytes);
@@ -789,12 +846,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t* sc32 = reinterpret_cast<const uint32_t*>(p.scales);  // ngroups and ess are even
         const int nsw_row = ngroups >> 1;
         uint32_t cc = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) {
-            int e, mt, nt, i0, nvalid;
-            item_coords(item, e, mt, nt, i0, nvalid);
-            const uint32_t* rows0 = sc32 + ((int64_t)e * p.ess + (int64_t)mt * kBM * ngroups) / 2;
+        Item I;
+        for (bool have = first_item(I); have; have = next_item(I)) {
+            const uint32_t* rows0 = sc32 + ((int64_t)I.e * p.ess + (int64_t)I.mt * kBM * ngroups) / 2;
             bool ok = true;
-            for (int c = 0; c < nchunks; ++c, ++cc) {
+            for (int c = I.c0; c < I.c1; ++c, ++cc) {
                 const int slot = cc % kChunkSlots;
                 if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 const int wlo = (c * CPC / G) >> 1;
@@ -829,10 +885,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t arow0 = smem_u32(sA) + r * 128 + (rx << 4);  // piece q of the A row: arow ^ (q << 4)
         uint32_t it = 0, cc = 0;
         bool ok = true;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        Item I;
+        for (bool have = first_item(I); have && ok; have = next_item(I)) {
             uint32_t crow = crow0, srow = srow0;
             int sub = 0, gbase = 0;
-            for (int kc = 0; kc < nk && ok; ++kc, ++it) {
+            const int ke = I.ke;
+            for (int kc = I.kb; kc < ke && ok; ++kc, ++it) {
                 if (sub == 0) {
                     const int slot = cc % kChunkSlots;
                     if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
@@ -871,7 +929,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                             const uint32_t w = WW[O + tt / F::kCW];
                             const uint32_t off =
                                 (sh >= kLog ? (w >> (sh - kLog)) : (w << (kLog - sh))) & (kMask * kStride);
-                            out[pp] = hmul2_bits<XT>(lds32(lutl + off), pp < 8 ? rr0 : rr1);
+                            out[pp] = hmul2_bits<XT>(lds32(lutl | off), pp < 8 ? rr0 : rr1);
                         }
                     };
                     using I0 = std::integral_constant<int, 0>;
@@ -897,7 +955,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     fence_async_smem();
                     mbar_arrive(full + s);
                 }
-                if (++sub == SPC || kc == nk - 1) {
+                if (++sub == SPC || kc == ke - 1) {
                     mbar_arrive(cempty + cc % kChunkSlots);
                     ++cc;
                     sub = 0;
@@ -909,25 +967,30 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int m = quarter * 32 + lane;
         uint32_t tile_it = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x, ++tile_it) {
-            int e, mt, nt, i0, nvalid;
-            item_coords(item, e, mt, nt, i0, nvalid);
+        if constexpr (SK) asm volatile("griddepcontrol.wait;" ::: "memory");  // y zeroed, scales written
+        Item I;
+        for (bool have = first_item(I); have; have = next_item(I), ++tile_it) {
+            const int mt = I.mt, i0 = I.i0, nvalid = I.nvalid;
             const int buf = tile_it & 1;
             if (!mbar_wait(tile_full + buf, (tile_it >> 1) & 1, abort_flag)) break;
             tc_fence_after();
             const int64_t ybase = (int64_t)i0 * p.rows + mt * kBM + m;
-            const bool ksplit = ((nvalid + 15) & ~15) <= 128 && nk >= 2;  // as the MMA threads decided
-            const uint32_t t0 = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kNT);
+            const bool ksplit = ((nvalid + 15) & ~15) <= 128 && I.ke - I.kb >= 2;  // as the MMA threads decided
+            const uint32_t t0 = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBuf);
+            // SK: partial sums of a run of chunks, added (y is f32 and zeroed beforehand)
+            auto put = [&](int c, float v) {
+                if (p.colscale) v *= __ldg(p.colscale + i0 + c);
+                if constexpr (SK) atomicAdd(static_cast<float*>(p.y) + ybase + (int64_t)c * p.rows, v);
+                else store_from_float(p.y, ybase + (int64_t)c * p.rows, p.ydt, v);
+            };
             if (ksplit) {
                 for (int c0 = 0; c0 < nvalid; c0 += 16) {  // the two K halves' partial sums
                     uint32_t v[16], w[16];
                     tc_ld16(t0 + (uint32_t)c0, v);
-                    tc_ld16(t0 + 128u + (uint32_t)c0, w);
+                    tc_ld16(t0 + (uint32_t)kHalf + (uint32_t)c0, w);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < nvalid)
-                            store_from_float(p.y, ybase + (int64_t)(c0 + j) * p.rows, p.ydt,
-                                             __uint_as_float(v[j]) + __uint_as_float(w[j]));
+                        if (c0 + j < nvalid) put(c0 + j, __uint_as_float(v[j]) + __uint_as_float(w[j]));
                 }
             } else {
                 for (int c0 = 0; c0 < nvalid; c0 += 32) {
@@ -935,8 +998,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     tc_ld32(t0 + (uint32_t)c0, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (c0 + j < nvalid)
-                            store_from_float(p.y, ybase + (int64_t)(c0 + j) * p.rows, p.ydt, __uint_as_float(v[j]));
+                        if (c0 + j < nvalid) put(c0 + j, __uint_as_float(v[j]));
                 }
             }
             tc_fence_before();
@@ -948,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (tid == 0 && *abort_flag && p.err) atomicOr(p.err, TQ_DEVERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kNT) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Q::kTmemCols) : "memory");
     }
 }
 
@@ -969,9 +1031,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
 }
 
-template <int LEVELS, int G>
+// Pair tiles and ring depths of the staged kernel: 256-pair tiles with 3 stages for
+// expert-sorted batches; for the dense split-K form, tiles of 16 or 64 pairs,
+// whose small B stages leave room for a deeper ring (the decode and MMA latencies
+// of a stage are about a thousand cycles each).
+constexpr int kSkSmallNT = 16, kSkSmallST = 8, kSkNT = 64, kSkST = 6;
+
+template <int LEVELS, int G, int NT = kNT, int ST = 3>
 size_t qmm2_smem_bytes(int experts) {
-    return (size_t)Q2Fmt<LEVELS, G>::kSmem + (size_t)(experts + 1) * 8;
+    return (size_t)Q2Fmt<LEVELS, G, NT, ST>::kSmem + (size_t)(experts + 1) * 8;
 }
 
 template <int LEVELS>
@@ -1049,9 +1117,111 @@ int sm_count() {
 template <int LEVELS, int G, int XT>
 tq_status launch_qmm2(const QmmParams& p, const QmmMaps& maps, cudaStream_t st) {
     const size_t smem = qmm2_smem_bytes<LEVELS, G>(p.experts);
-    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, XT>, smem) != cudaSuccess) return TQ_ERR_CUDA;
-    gather_qmm2_kernel<LEVELS, G, XT><<<sm_count(), kThreads2, smem, st>>>(p, maps);
+    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, XT, kNT, 3, false>, smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    gather_qmm2_kernel<LEVELS, G, XT, kNT, 3, false><<<sm_count(), kThreads2, smem, st>>>(p, maps);
     return launch_status();
+}
+
+// Dense split-K form (fp16 operands): one CTA per SM at most, each over a
+// contiguous range of the (row tile, code chunk) units.
+template <int LEVELS, int G, int NT, int ST>
+tq_status launch_sk(const QmmParams& p, const QmmMaps& maps, cudaStream_t st) {
+    using Q = Q2Fmt<LEVELS, G, NT, ST>;
+    const size_t smem = qmm2_smem_bytes<LEVELS, G, NT, ST>(1);
+    if (smem > (size_t)kSmemLimit) return TQ_ERR_UNSUPPORTED;
+    const int units = (p.rows / kBM) * ((p.cols / kBK + Q::kSPC - 1) / Q::kSPC);
+    const int grid = units < sm_count() ? units : sm_count();
+    if (ensure_smem((const void*)gather_qmm2_kernel<LEVELS, G, 0, NT, ST, true>, smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    // Programmatic dependent launch: the prologue and the first code chunks overlap the prep
+    // kernel; only the input-row copies and the epilogue wait for it (griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads2);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, gather_qmm2_kernel<LEVELS, G, 0, NT, ST, true>, p, maps);
+    return launch_status();
+}
+
+template <int LEVELS, int G>
+tq_status launch_sk_nt(const QmmParams& p, const QmmMaps& maps, cudaStream_t st) {
+    return p.P <= kSkSmallNT ? launch_sk<LEVELS, G, kSkSmallNT, kSkSmallST>(p, maps, st)
+                             : launch_sk<LEVELS, G, kSkNT, kSkST>(p, maps, st);
+}
+
+template <int LEVELS>
+tq_status launch_sk_g(const QmmParams& p, int group, const QmmMaps& maps, cudaStream_t st) {
+    switch (group) {
+        case 16: return launch_sk_nt<LEVELS, 16>(p, maps, st);
+        case 32: return launch_sk_nt<LEVELS, 32>(p, maps, st);
+        case 64: return launch_sk_nt<LEVELS, 64>(p, maps, st);
+        case 128: return launch_sk_nt<LEVELS, 128>(p, maps, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
+// x (f32 [T, cols], cols a multiple of 64) -> x16 = fp16(x / 2^e_t) with 2^e_t the power of
+// two just above max |x[t, :]| (colscale[t] = 2^e_t, so the outputs of row t are scaled back
+// exactly), one block per input row, four 16-byte loads in flight per thread; the remaining
+// blocks zero y (f32, ny values) for the split-K sums.  The dependent matvec may launch at once.
+TQ_DEVFN float4 ld_row4(const float* r, int i, bool v4) {
+    if (v4) return __ldg(reinterpret_cast<const float4*>(r) + i);
+    return make_float4(__ldg(r + 4 * i), __ldg(r + 4 * i + 1), __ldg(r + 4 * i + 2), __ldg(r + 4 * i + 3));
+}
+
+__global__ void __launch_bounds__(256) qmv_tc_prep_kernel(const float* __restrict__ x, int T, int cols,
+                                                          __half* __restrict__ x16, float* __restrict__ colscale,
+                                                          float* __restrict__ y, int64_t ny) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ float red[8];
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x >= T) {
+        const int64_t n0 = (int64_t)(blockIdx.x - T) * blockDim.x + tid, step = (int64_t)(gridDim.x - T) * blockDim.x;
+        for (int64_t i = n0; i < ny; i += step) y[i] = 0.f;
+        return;
+    }
+    const float* xr = x + (int64_t)blockIdx.x * cols;
+    const bool v4 = (reinterpret_cast<uintptr_t>(xr) & 15) == 0;
+    const int n4 = cols / 4, nt = blockDim.x;
+    float m = 0.f;
+    for (int i0 = tid; i0 < n4; i0 += 4 * nt) {
+        float4 v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = i0 + t * nt < n4 ? ld_row4(xr, i0 + t * nt, v4) : make_float4(0, 0, 0, 0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v[t].x), fabsf(v[t].y)), fmaxf(fabsf(v[t].z), fabsf(v[t].w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    m = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    int e = 0;
+    if (m > 0.f && m <= 3.4e38f) frexpf(m, &e);  // m = f * 2^e, f in [0.5, 1): |x| / 2^e < 1
+    const float inv = ldexpf(1.f, -e);
+    if (tid == 0) colscale[blockIdx.x] = ldexpf(1.f, e);
+    uint2* dr = reinterpret_cast<uint2*>(x16 + (int64_t)blockIdx.x * cols);  // 4 halves per 8 bytes
+    for (int i0 = tid; i0 < n4; i0 += 4 * nt) {
+        float4 v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = i0 + t * nt < n4 ? ld_row4(xr, i0 + t * nt, v4) : make_float4(0, 0, 0, 0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (i0 + t * nt < n4) {
+                __half2 a = __floats2half2_rn(v[t].x * inv, v[t].y * inv), b = __floats2half2_rn(v[t].z * inv, v[t].w * inv);
+                dr[i0 + t * nt] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+            }
+        }
+    }
 }
 
 template <int LEVELS, int G, int XT>
@@ -1142,5 +1312,59 @@ extern "C" tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtyp
         case 8: return dispatch_g<8>(p, w->group, xt, mp, st);
         case 16: return dispatch_g<16>(p, w->group, xt, mp, st);
         default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
+extern "C" size_t tq_qmv_tc_workspace_bytes(int32_t T, int32_t cols) {
+    if (T <= 0 || cols <= 0) return 0;
+    return ((size_t)T * (size_t)cols * 2 + 15) / 16 * 16 + ((size_t)T * 4 + 15) / 16 * 16;
+}
+
+extern "C" tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_t T, float* y, void* ws,
+                               size_t ws_bytes, void* stream) {
+    if (!w || !w->codes || !w->scales || !w->cb.centroids) return TQ_ERR_INVALID;
+    if (w->experts <= 0 || w->rows <= 0 || w->cols <= 0) return TQ_ERR_INVALID;
+    if (!(w->group == 16 || w->group == 32 || w->group == 64 || w->group == 128) || w->cols % w->group)
+        return TQ_ERR_INVALID;
+    if (w->row_stride_words < tq_row_words(w->cb.levels, w->cols)) return TQ_ERR_INVALID;
+    if (T < 0) return TQ_ERR_INVALID;
+    if (T == 0) return TQ_OK;
+    if (!x_rot || !y) return TQ_ERR_INVALID;
+    if (!(w->cb.levels == 4 || w->cb.levels == 8 || w->cb.levels == 16)) return TQ_ERR_UNSUPPORTED;
+    if (w->rows % kBM || w->cols % kBK || T > kSkNT) return TQ_ERR_UNSUPPORTED;
+    const size_t need = tq_qmv_tc_workspace_bytes(T, w->cols);
+    if (!ws || ws_bytes < need || !aligned(ws, 16)) return TQ_ERR_INVALID;
+    QmmParams p{};
+    p.codes = w->codes;
+    p.scales = w->scales;
+    p.row_stride = w->row_stride_words;
+    p.esw = 0;
+    p.ess = 0;
+    p.rows = w->rows;
+    p.cols = w->cols;
+    p.experts = 1;  // the dense matrix is expert 0
+    p.centroids = w->cb.centroids;
+    __half* x16 = static_cast<__half*>(ws);
+    float* cs = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((size_t)T * w->cols * 2 + 15) / 16 * 16);
+    p.x = x16;
+    p.P = T;
+    p.k = 1;
+    p.per_pair = 1;
+    p.y = y;
+    p.ydt = TQ_F32;
+    p.colscale = cs;
+    if (!staged_fits(p, w->group, w->cb.levels)) return TQ_ERR_UNSUPPORTED;
+    QmmMaps maps;
+    if (!encode_maps(p, x16, maps)) return TQ_ERR_CUDA;
+    cudaStream_t st = as_stream(stream);
+    const int64_t ny = (int64_t)T * w->rows;
+    const int zb = (int)std::min<int64_t>((ny + 255) / 256, 4 * (int64_t)sm_count());
+    qmv_tc_prep_kernel<<<T + zb, 256, 0, st>>>(x_rot, T, w->cols, x16, cs, y, ny);
+    const tq_status s = launch_status();
+    if (s != TQ_OK) return s;
+    switch (w->cb.levels) {
+        case 4: return launch_sk_g<4>(p, w->group, maps, st);
+        case 8: return launch_sk_g<8>(p, w->group, maps, st);
+        default: return launch_sk_g<16>(p, w->group, maps, st);
     }
 }

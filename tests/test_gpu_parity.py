@@ -123,8 +123,9 @@ def test_quantize_then_qmv(lib, levels, group, K, block, rows, wdt, T):
     x = wl.rng(5, T, K).normal(size=(T, K)).astype(np.float32)
     xr = lib.rotate(_dev(x), e["rot"])
     qw = lib.QWeight(e["codes"], e["scales"], 1, rows, K, group, e["cb"])
-    y = lib.qmv(qw, xr).cpu().numpy()
     ref = o.qmv(o.dequantize(e["ocodes"], e["os16"], e["oc"], group), o.rotate(x, e["signs"], block))
+    assert rel_l2(lib.qmv(qw, xr).cpu().numpy(), ref) < REL_L2  # the tensor-core form where it applies
+    y = lib.qmv(qw, xr, tensor_cores=False).cpu().numpy()
     assert rel_l2(y, ref) < REL_L2
     # bf16 output: the kernel's own fp32 result rounded once (nearest even), and
     # within the bar of the oracle rounded to bf16 the same way.
@@ -185,9 +186,61 @@ def test_qmv_decode_exact(lib, levels, group, K, rows):
     qw, Wh = _bank_dev(lib, levels, 1, rows, K, group, seed=levels * 100 + group)
     x = wl.rng(3, K).normal(size=(4, K))
     for T in (1, 2, 4):
-        y = lib.qmv(qw, _dev(x[:T].astype(np.float32))).cpu().numpy()
+        y = lib.qmv(qw, _dev(x[:T].astype(np.float32)), tensor_cores=False).cpu().numpy()
         ref = o.qmv(Wh(0), x[:T].astype(np.float32))
         assert rel_l2(y, ref) < _decode_tol(levels), T
+
+
+# Tensor-core dense matvec: fp16 operands (unit roundoff u = 2^-11 each for the
+# scaled input and the decoded weight), fp32 sums.  Per product the relative error
+# has a standard deviation of about sqrt(2/3) u = 4e-4 and the errors are
+# independent, so the relative L2 error of y stays near that; 1e-3 is the bar.
+TC_TOL = 1e-3
+
+
+@pytest.mark.parametrize("levels,group,K,rows,Ts", [
+    (8, 128, 4096, 256, (1, 3, 16, 17, 64)),  # the dense decode shape, 2 row tiles, both pair tiles
+    (8, 128, 4096, 2048, (4,)),               # 208 units over the SMs: CTA ranges cross row tiles
+    (8, 32, 1344, 128, (2, 13)),              # 21 stages: the last code chunk holds one stage
+    (16, 64, 1024, 384, (5,)),                # 4-bit, 3 row tiles
+    (4, 32, 2048, 128, (1, 8)),               # 2-bit, 64 groups a row
+    (8, 16, 1024, 256, (16,)),                # group 16
+])
+def test_qmv_tensor_cores(lib, levels, group, K, rows, Ts):
+    qw, Wh = _bank_dev(lib, levels, 1, rows, K, group, seed=levels * 7 + group)
+    W = Wh(0)
+    for T in Ts:
+        x = wl.rng(8, T, K).normal(size=(T, K)).astype(np.float32)
+        y = lib.qmv_tc(qw, _dev(x)).cpu().numpy()
+        assert rel_l2(y, o.qmv(W, x)) < TC_TOL, T
+
+
+def test_qmv_tensor_cores_input_range(lib):
+    """Rows of very different magnitude, and a zero row: each row is scaled by its own power of two
+    (fp16 alone would overflow at 1e6 and flush 1e-7 to zero)."""
+    qw, Wh = _bank_dev(lib, 8, 1, 256, 1024, 64, seed=3)
+    W = Wh(0)
+    x = wl.rng(9, 4).normal(size=(4, 1024)).astype(np.float32)
+    x[0] *= 1e6
+    x[2] *= 1e-7
+    x[3] = 0.0
+    y = lib.qmv_tc(qw, _dev(x)).cpu().numpy()
+    ref = o.qmv(W, x)
+    for t in range(3):
+        assert rel_l2(y[t], ref[t]) < TC_TOL, t
+    assert not np.any(y[3])
+
+
+def test_qmv_tensor_cores_unsupported_shapes(lib):
+    """Shapes outside the form raise (nothing launched); qmv() then takes tq_qmv."""
+    qw, Wh = _bank_dev(lib, 8, 1, 130, 1024, 64, seed=4)  # rows not a multiple of 128
+    x = wl.rng(10, 2).normal(size=(2, 1024)).astype(np.float32)
+    with pytest.raises(lib.TQError):
+        lib.qmv_tc(qw, _dev(x))
+    assert rel_l2(lib.qmv(qw, _dev(x)).cpu().numpy(), o.qmv(Wh(0), x)) < 1e-5
+    qw3, _ = _bank_dev(lib, 3, 1, 128, 1024, 64, seed=4)  # ternary book
+    with pytest.raises(lib.TQError):
+        lib.qmv_tc(qw3, _dev(x))
 
 
 def test_gather_qmv_and_bad_ids(lib):
