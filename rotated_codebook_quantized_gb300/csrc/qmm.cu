@@ -154,7 +154,7 @@ struct QmmParams {
     void* y;
     int ydt;
     uint32_t* err;
-    const float* colscale;  // per pair row of x: factor applied to its outputs (may be null)
+    const float* colscale;  // split-K form: per input row, the factor applied to its outputs
 };
 
 template <int LEVELS, int G, int XT>
@@ -631,13 +631,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int ngroups = p.cols / G;
     const int nchunks = (nk + SPC - 1) / SPC;
 
-    if constexpr (!SK)
+    if constexpr (!SK) {
         for (int i = tid; i <= E; i += kThreads2) cum[i] = offs[i] = p.offsets[i];
-    for (int i = tid; i < NL * COPIES; i += kThreads2) {
-        const int idx = i / COPIES;
-        lut[i] = pack2<XT>(p.centroids[idx & (LEVELS - 1)], p.centroids[idx / LEVELS]);
+        __syncthreads();
     }
-    __syncthreads();
     if (tid == 0) {
         if constexpr (SK) {
             *total_items = mtiles * nchunks;  // units
@@ -680,16 +677,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (tid == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
         return;
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(Q::kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // The code and scale warps start their copies at once; the others fill the table and
+    // allocate TMEM, then meet at a named barrier (the copying warps use neither).
+    uint32_t tmem = 0;
+    if (warp != kCodeWarp && warp != kScaleWarp) {
+        const int ftid = warp < kCodeWarp ? tid : tid - 64;
+        for (int i = ftid; i < NL * COPIES; i += kThreads2 - 64) {
+            const int idx = i / COPIES;
+            lut[i] = pack2<XT>(p.centroids[idx & (LEVELS - 1)], p.centroids[idx / LEVELS]);
+        }
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(Q::kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"r"(kThreads2 - 64) : "memory");
+        tc_fence_after();
+        tmem = *tmem_slot;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     // One item: chunks [c0, c1) (stages [kb, ke)) of row tile mt of expert e against pair
     // tile nt (pairs i0 .. i0 + nvalid - 1).  Every role walks the same item sequence.
@@ -883,24 +891,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t srow0 = smem_u32(sC) + kChunkCodeBytes + r * (SW * 4);  // word j: srow + ((j ^ sx) << 2)
         const int sx = (r / (32 / SW)) & (SW - 1);
         const uint32_t arow0 = smem_u32(sA) + r * 128 + (rx << 4);  // piece q of the A row: arow ^ (q << 4)
+        // The stage counter it runs over every stage of the CTA; this group decodes those with
+        // (it & 1) == grp.  Each code chunk is waited for once and released once by every
+        // decoder thread; the empty barrier of the group's next stage is tested before the
+        // current stage is decoded, so that its latency overlaps the decode.
         uint32_t it = 0, cc = 0;
-        bool ok = true;
+        bool ok = true, pre = false;  // pre: the empty test of the next stage succeeded
         Item I;
         for (bool have = first_item(I); have && ok; have = next_item(I)) {
-            uint32_t crow = crow0, srow = srow0;
-            int sub = 0, gbase = 0;
-            const int ke = I.ke;
-            for (int kc = I.kb; kc < ke && ok; ++kc, ++it) {
-                if (sub == 0) {
-                    const int slot = cc % kChunkSlots;
-                    if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
-                    crow = crow0 + slot * kChunkBytes;
-                    srow = srow0 + slot * kChunkBytes;
-                    gbase = ((kc / SPC) * CPC / G) & ~1;  // group at word 0 of the chunk's scale rows
-                }
-                if ((int)(it & 1) == grp) {
-                    const int s = it % kStages;
-                    if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            for (int c = I.c0; c < I.c1 && ok; ++c, ++cc) {
+                const int k0 = c * SPC, nsub = min(SPC, I.ke - k0);
+                const int slot = cc % kChunkSlots;
+                if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
+                const uint32_t crow = crow0 + slot * kChunkBytes, srow = srow0 + slot * kChunkBytes;
+                const int gbase = (c * CPC / G) & ~1;  // group at word 0 of the chunk's scale rows
+                for (int sub = (int)((it ^ (uint32_t)grp) & 1u); sub < nsub; sub += 2) {
+                    const uint32_t sit = it + (uint32_t)sub;
+                    const int kc = k0 + sub;
+                    const int s = sit % kStages;
+                    if (!pre && !mbar_wait(empty + s, ((sit / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    {
+                        const uint32_t nit = sit + 2;  // this group's next stage
+                        pre = mbar_peek(empty + nit % kStages, ((nit / kStages) & 1) ^ 1);
+                    }
                     const int lq = 64 * sub + 32 * h;  // first code of this thread within the chunk
                     const int w0 = lq / F::kCW, pos0 = lq - w0 * F::kCW;
                     const int o = w0 & 3, q0 = w0 >> 2;
@@ -955,11 +968,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     fence_async_smem();
                     mbar_arrive(full + s);
                 }
-                if (++sub == SPC || kc == ke - 1) {
-                    mbar_arrive(cempty + cc % kChunkSlots);
-                    ++cc;
-                    sub = 0;
-                }
+                if (!ok) break;
+                it += (uint32_t)nsub;
+                mbar_arrive(cempty + slot);
             }
         }
     } else {
@@ -979,9 +990,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const uint32_t t0 = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBuf);
             // SK: partial sums of a run of chunks, added (y is f32 and zeroed beforehand)
             auto put = [&](int c, float v) {
-                if (p.colscale) v *= __ldg(p.colscale + i0 + c);
-                if constexpr (SK) atomicAdd(static_cast<float*>(p.y) + ybase + (int64_t)c * p.rows, v);
-                else store_from_float(p.y, ybase + (int64_t)c * p.rows, p.ydt, v);
+                if constexpr (SK) {  // the per-row input scale of the prep kernel, then a partial sum
+                    atomicAdd(static_cast<float*>(p.y) + ybase + (int64_t)c * p.rows, v * __ldg(p.colscale + i0 + c));
+                } else {
+                    store_from_float(p.y, ybase + (int64_t)c * p.rows, p.ydt, v);
+                }
             };
             if (ksplit) {
                 for (int c0 = 0; c0 < nvalid; c0 += 16) {  // the two K halves' partial sums

@@ -945,7 +945,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             for (;;) {
                 if (__all_sync(kFull, done)) break;
                 const int slot = lane * D + (int)(uses % D);
-                const bool ready = !done && mbar_test(empty + slot, ((uses / D) & 1) ^ 1);
+                const bool ready = !done && mbar_peek(empty + slot, ((uses / D) & 1) ^ 1);
                 const unsigned rmask = __ballot_sync(kFull, ready);
                 if (ready) {
                     const int j = next + __popc(rmask & ((1u << lane) - 1));

@@ -41,11 +41,24 @@ TQ_DEVFN bool mbar_wait_drain(uint64_t* b, uint32_t parity) {
     return true;
 }
 
-// Has the phase of parity `parity` completed?  (No suspension.)
+// Has the phase of parity `parity` completed?  (try_wait without a time hint: when the phase
+// is not complete the thread may still be held for a system-dependent time; mbar_peek never is.)
 TQ_DEVFN bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe of the phase (mbarrier.test_wait never suspends the thread, unlike
+// try_wait, which may wait for the phase up to a system-dependent time).
+TQ_DEVFN bool mbar_peek(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(b)), "r"(parity)
         : "memory");
