@@ -2,11 +2,12 @@
 
 Workload: one MoE decode step = route 1 token over 384 experts (top-8, fp32
 logits), rotate its bf16 [1, 7168] input, gate||up gather-qmv over the 8
-routed ternary experts (group 16, 20 trits per word), down multi-gather-qmv
-with the SwiGLU and the rotation of the 2048-wide intermediate done inside
-it, router-weighted combine.  The
-metric is packed-weight bytes read per second by the step (codes + fp16 scales
-of the 8 routed experts, 114,720,768 B per step).
+routed ternary experts (group 16, 20 trits per word), SwiGLU + rotation of the
+2048-wide intermediate, down multi-gather-qmv, router-weighted combine (six
+launches; the forms with the SwiGLU, or also the input rotation, inside the
+matvec are timed beside it as step_variants).  The metric is packed-weight
+bytes read per second by the step (codes + fp16 scales of the 8 routed
+experts, 114,720,768 B per step).
 
 Timing: inputs resident in HBM; each timed step is one CUDA-graph replay of the
 whole step between two CUDA events, with a 256 MiB L2 flush before every step
@@ -247,8 +248,10 @@ def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
                        "min_pairs_per_expert": int(counts.min())}}
 
 
-def graph_time_us(torch, fn, flush, iters=20, skip=3):
-    """Median device time (us) of one CUDA-graph replay of fn(), L2 flushed before each replay."""
+def graph_time_us(torch, fn, flush, iters=40, skip=4):
+    """Device time (us) of one CUDA-graph replay of fn(), L2 flushed before each replay: the mean
+    of the middle 60 % of the replays after warm-up (the event timer ticks in steps of about
+    2 us, so averaging, not a median, resolves differences below a tick)."""
     dev = flush.device
     fn()
     torch.cuda.synchronize()
@@ -267,7 +270,9 @@ def graph_time_us(torch, fn, flush, iters=20, skip=3):
         ev[i][1].record()
     torch.cuda.synchronize()
     t = sorted(ev[i][0].elapsed_time(ev[i][1]) for i in range(skip, iters))
-    return t[len(t) // 2] * 1e3
+    cut = len(t) // 5
+    mid = t[cut:len(t) - cut]
+    return sum(mid) / len(mid) * 1e3
 
 
 def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
@@ -411,11 +416,19 @@ def main():
     logits_buf = torch.empty((1, nexp), dtype=torch.float32, device=dev)
     x_buf = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device=dev)
 
-    def step():
+    def step():  # six calls, one per hot-path step
         ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)  # decode reads experts by id
         xr = tq.rotate(x_buf, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
-        yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))  # SwiGLU + rotation inside
+        hr = tq.swiglu_rotate(gu, INTER, rotI)
+        yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
+        return tq.moe_combine(yd, probs, TOPK)
+
+    def step_fused_down():  # SwiGLU + rotation inside the down matvec (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
+        xr = tq.rotate(x_buf, rotH)
+        gu = tq.gather_qmv(qgu, xr, ids)
+        yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
     def step_all_fused():  # the input rotation inside gate||up too (measured, not the headline)
@@ -424,15 +437,7 @@ def main():
         yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    def step_separate():  # six separate calls, one per hot-path step (measured, not the headline)
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
-        xr = tq.rotate(x_buf, rotH)
-        gu = tq.gather_qmv(qgu, xr, ids)
-        hr = tq.swiglu_rotate(gu, INTER, rotI)
-        yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
-        return tq.moe_combine(yd, probs, TOPK)
-
-    launches_per_step = 5  # route top-k; rotate; gate||up gather; down multi-gather with SwiGLU; combine
+    launches_per_step = 6  # route top-k; rotate; gate||up gather; SwiGLU + rotate; down multi-gather; combine
 
     # warm up eagerly (first calls set kernel attributes), then capture the step
     logits_buf.copy_(logits_all[0:1])
@@ -545,8 +550,8 @@ def main():
     # the same step with other splits into calls (same inputs; one graph replay each, L2 flushed)
     step_variants = None
     if not args.skip_extras:
-        step_variants = {"headline_5_launches_us": graph_time_us(torch, step, flush),
-                         "separate_6_launches_us": graph_time_us(torch, step_separate, flush),
+        step_variants = {"headline_6_launches_us": graph_time_us(torch, step, flush),
+                         "swiglu_in_down_5_launches_us": graph_time_us(torch, step_fused_down, flush),
                          "rotation_in_gate_up_too_4_launches_us": graph_time_us(torch, step_all_fused, flush)}
     extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
 

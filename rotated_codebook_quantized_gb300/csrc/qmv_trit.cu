@@ -874,7 +874,11 @@ TQ_DEVFN void unit_scales(uint32_t a, uint32_t sh, float (&s)[5]) {
     s[4] = __low2float(*reinterpret_cast<const __half2*>(&v2));
 }
 
+// XS: the kernel carries the input stage (xmode 1 or 2); without it (xmode 0) none of that code
+// or its registers is in the plain matvec.
+template <bool XS>
 __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritParams tp, const __grid_constant__ TritMaps maps) {
+    const int xmode = XS ? tp.xmode : 0;
     constexpr int G = 16;
     using F = TritFmt<G>;
     constexpr int GPU = 5, S = kTcS, US = kTcUS, D = kTcDepth, NC = kTcWarps, RT = kTcRows;
@@ -897,7 +901,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kTcSlots);
     int* tag = reinterpret_cast<int*>(empty + kTcSlots + 1);            // [slots]: (task << 8) | stage, or -1
     float* xf = reinterpret_cast<float*>(tag + (kTcSlots + 3) / 4 * 4);  // [cols / 32][33] input stage (xmode != 0)
-    float* rowsum = xf + (tp.xmode ? (p.cols / 32) * 33 : 0);             // [tasks of this CTA][RT]
+    float* rowsum = xf + (xmode ? (p.cols / 32) * 33 : 0);             // [tasks of this CTA][RT]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t_begin = (int)((int64_t)blockIdx.x * tp.total_tasks / gridDim.x);
@@ -1006,7 +1010,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             const int q = q0 + ctid + r * NCT;
             if (q < nq) {
                 sg[r] = __ldg(sg4 + q);
-                if (tp.xmode == 1) {
+                if (xmode == 1) {
                     if (tp.xdt == TQ_F32) {
                         xv4[r] = __ldg(reinterpret_cast<const float4*>(tp.xin) + vec * nq + q);
                     } else {
@@ -1025,14 +1029,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
     };
     float4 pre_x[4];
     uint32_t pre_sg[4];
-    const int64_t pre_vec = tp.xmode != 0 && t_begin < t_end && nq <= 4 * NCT ? vec_of(t_begin / tpi) : -1;
+    const int64_t pre_vec = xmode != 0 && t_begin < t_end && nq <= 4 * NCT ? vec_of(t_begin / tpi) : -1;
     if (pre_vec >= 0) load_quads(pre_vec, 0, pre_x, pre_sg);  // in flight while the table is built
     if (t_begin < t_end) {  // start fetching the first input vector while the table is built
         const int64_t v0 = vec_of(t_begin / tpi);
-        const int64_t bytes = tp.xmode == 0 ? (int64_t)p.cols * 4
-                              : tp.xmode == 1 ? (int64_t)p.cols * (tp.xdt == TQ_F32 ? 4 : 2)
+        const int64_t bytes = xmode == 0 ? (int64_t)p.cols * 4
+                              : xmode == 1 ? (int64_t)p.cols * (tp.xdt == TQ_F32 ? 4 : 2)
                                               : (int64_t)p.cols * 8;  // [gate | up] in f32
-        const char* x0 = tp.xmode == 0 ? reinterpret_cast<const char*>(p.x) : reinterpret_cast<const char*>(tp.xin);
+        const char* x0 = xmode == 0 ? reinterpret_cast<const char*>(p.x) : reinterpret_cast<const char*>(tp.xin);
         x0 += v0 * bytes;
         for (int64_t off = ctid * 128; off < bytes; off += NCT * 128)
             asm volatile("prefetch.global.L1 [%0];" ::"l"(x0 + off));
@@ -1076,7 +1080,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             auto pack = [](int qlo, int qhi) { return ((uint32_t)qhi & 0xffffu) | ((uint32_t)qlo << 16); };
             constexpr int kV4 = 4;  // 16-byte input loads per thread when the vector fits
             const int nv4 = p.cols >> 2;
-            if (tp.xmode != 0) {
+            if (xmode != 0) {
                 // The input stage: x (or silu(gate) * up) times the signs, into rows of 32 floats
                 // padded to 33, then the block Hadamard transform of the rotation as 32-point
                 // transforms along the rows and M-point transforms down the columns of every
@@ -1194,7 +1198,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
                     xb[pair_at(k)] = pack(__float2int_rn(lo * inv), __float2int_rn(hi * inv));
                 }
             }
-            if (has_off && tp.xmode == 0) {
+            if (has_off && xmode == 0) {
                 for (int g = ctid; g < nunits_pad * GPU; g += NCT) {
                     float sum = 0.f;
                     for (int k = g * G; k < min((g + 1) * G, p.cols); ++k) sum += __ldg(xv + k);
@@ -1369,9 +1373,13 @@ tq_status launch_trit_tc(const QmvParams& qp, int n_items, cudaStream_t st, cons
     if (smem > 227 * 1024) return TQ_ERR_UNSUPPORTED;
     TritMaps maps;
     if (!encode_trit_maps(qp, maps)) return TQ_ERR_UNSUPPORTED;
-    const void* kfn = (const void*)qmv_trit_tc_kernel;
-    if (ensure_smem(kfn, smem) != cudaSuccess) return TQ_ERR_CUDA;
-    qmv_trit_tc_kernel<<<(unsigned)grid, kTcThreads, smem, st>>>(tp, maps);
+    if (tp.xmode) {
+        if (ensure_smem((const void*)qmv_trit_tc_kernel<true>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+        qmv_trit_tc_kernel<true><<<(unsigned)grid, kTcThreads, smem, st>>>(tp, maps);
+    } else {
+        if (ensure_smem((const void*)qmv_trit_tc_kernel<false>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+        qmv_trit_tc_kernel<false><<<(unsigned)grid, kTcThreads, smem, st>>>(tp, maps);
+    }
     return launch_status();
 }
 
