@@ -4,15 +4,16 @@ Workload: one MoE decode step = route 1 token over 384 experts (top-8, fp32
 logits), rotate its bf16 [1, 7168] input, gate||up gather-qmv over the 8
 routed ternary experts (group 16, 20 trits per word), SwiGLU + rotation of the
 2048-wide intermediate, down multi-gather-qmv, router-weighted combine (six
-launches; the forms with the SwiGLU, or also the input rotation, inside the
-matvec are timed beside it as step_variants).  The metric is packed-weight
-bytes read per second by the step (codes + fp16 scales of the 8 routed
-experts, 114,720,768 B per step).
+launches, routing and the input rotation side by side on two streams; the
+same six in one stream, and the forms with the SwiGLU, or also the input
+rotation, inside the matvec are timed beside it as step_variants).  The metric
+is packed-weight bytes read per second by the step (codes + fp16 scales of the
+8 routed experts, 114,720,768 B per step).
 
 Timing: inputs resident in HBM; each timed step is one CUDA-graph replay of the
 whole step between two CUDA events, with a 256 MiB L2 flush before every step
 (outside the events) and a 5.5 GB expert bank, so every step reads its experts
-from HBM.  ``e2e`` repeats the step through the Python API with the step's
+from HBM.  ``e2e`` repeats the step (eagerly, in one stream) through the Python API with the step's
 inputs copied from pinned host memory and its output copied back.
 
 Also measured: the gate||up gather-qmv launch alone (roofline of the dominant
@@ -416,8 +417,22 @@ def main():
     logits_buf = torch.empty((1, nexp), dtype=torch.float32, device=dev)
     x_buf = torch.empty((1, HIDDEN), dtype=torch.bfloat16, device=dev)
 
-    def step():  # six calls, one per hot-path step
+    aux = torch.cuda.Stream(device=dev)
+
+    def step():  # six calls, one per hot-path step; routing and the input rotation run side by side
+        cur = torch.cuda.current_stream()
+        aux.wait_stream(cur)
+        with torch.cuda.stream(aux):
+            xr = tq.rotate(x_buf, rotH)
         ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)  # decode reads experts by id
+        cur.wait_stream(aux)
+        gu = tq.gather_qmv(qgu, xr, ids)
+        hr = tq.swiglu_rotate(gu, INTER, rotI)
+        yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
+        return tq.moe_combine(yd, probs, TOPK)
+
+    def step_serial():  # the same six calls in one stream (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
         xr = tq.rotate(x_buf, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
         hr = tq.swiglu_rotate(gu, INTER, rotI)
@@ -533,7 +548,7 @@ def main():
         logits_buf.copy_(h_logits[i:i + 1], non_blocking=True)
         d_x.copy_(h_x[i:i + 1], non_blocking=True)
         x_buf.copy_(d_x.view(torch.bfloat16))
-        out = step()
+        out = step_serial()  # eager: the stream fork and join of the graph's step cost more host time than they save
         h_out[i:i + 1].copy_(out, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -551,6 +566,7 @@ def main():
     step_variants = None
     if not args.skip_extras:
         step_variants = {"headline_6_launches_us": graph_time_us(torch, step, flush),
+                         "one_stream_6_launches_us": graph_time_us(torch, step_serial, flush),
                          "swiglu_in_down_5_launches_us": graph_time_us(torch, step_fused_down, flush),
                          "rotation_in_gate_up_too_4_launches_us": graph_time_us(torch, step_all_fused, flush)}
     extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
