@@ -133,8 +133,11 @@ TQ_DEVFN uint32_t trit_next_int(uint32_t& F) {
 // with i ^ h (the Sylvester order).  Stages inside a thread run in registers,
 // stages within a warp use shuffles, the rest go through shared memory `s`
 // (at least nthreads*E floats).  All threads of the CTA must call it.
+// Floats of shared memory fwht_cta needs for n elements (one pad float per 32).
+inline __host__ __device__ constexpr size_t fwht_pad_floats(size_t n) { return n + n / 32; }
+
 template <int E>
-TQ_DEVFN void fwht_cta(float (&v)[E], float* s, int block) {
+TQ_DEVFN void fwht_cta(float (&v)[E], float* s, int block) {  // s: fwht_pad_floats(threads * E) floats
     const int lane = threadIdx.x & 31;
     int h = 1;
 #pragma unroll
@@ -161,15 +164,17 @@ TQ_DEVFN void fwht_cta(float (&v)[E], float* s, int block) {
         }
     }
     if (h < block) {
+        // Element i sits at i + i / 32: a thread's E consecutive elements would otherwise put
+        // the lanes of one access E floats apart, an E-way bank conflict (fwht_pad_floats).
         const int base = threadIdx.x * E;
         for (; h < block; h <<= 1) {
 #pragma unroll
-            for (int i = 0; i < E; ++i) s[base + i] = v[i];
+            for (int i = 0; i < E; ++i) s[(base + i) + ((base + i) >> 5)] = v[i];
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                const int idx = base + i;
-                float o = s[idx ^ h];
+                const int idx = base + i, j = idx ^ h;
+                float o = s[j + (j >> 5)];
                 v[i] = (idx & h) ? (o - v[i]) : (v[i] + o);
             }
             __syncthreads();

@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
                                                              uint32_t* __restrict__ codes, uint16_t* __restrict__ scales,
                                                              int64_t row_stride) {
     extern __shared__ float smem[];
-    float* fw = smem;                                           // cols floats (FWHT exchange)
-    float* thr = smem + cols;                                   // levels-1 thresholds
+    float* fw = smem;                                           // fwht_pad_floats(cols) (FWHT exchange)
+    float* thr = smem + fwht_pad_floats(cols);                  // levels-1 thresholds
     uint8_t* cd = reinterpret_cast<uint8_t*>(thr + 256);        // cols codes
     const int64_t row = blockIdx.x;
     const int base = threadIdx.x * E;
@@ -66,8 +66,27 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
     for (int i = threadIdx.x; i < nthr; i += blockDim.x) thr[i] = thresholds[i];
 
     float v[E];
+    const int64_t off = row * cols + base;
+    if (E >= 8 && wdt == TQ_BF16 && (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (cols & 7) == 0 &&
+        (reinterpret_cast<uintptr_t>(signs) & 7) == 0) {
+        // 8 values and 8 signs per 16-byte / 8-byte load
 #pragma unroll
-    for (int i = 0; i < E; ++i) v[i] = load_as_float(W, row * cols + base + i, wdt) * (float)signs[base + i];
+        for (int c = 0; c < E; c += 8) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(W) + off + c));
+            const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + base + c));
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t s2[2] = {sg.x, sg.y};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t bits = k & 1 ? (w4[k >> 1] & 0xffff0000u) : (w4[k >> 1] << 16);
+                const int sgn = (int)(int8_t)(s2[k >> 2] >> (8 * (k & 3)));
+                v[c + k] = __uint_as_float(bits) * (float)sgn;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[i] = load_as_float(W, off + i, wdt) * (float)signs[base + i];
+    }
     fwht_cta<E>(v, fw, block);  // ends with a barrier when it used shared memory
     __syncthreads();
 #pragma unroll
@@ -75,13 +94,16 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
 
     const float inv_g = 1.0f / (float)group;
     const int ngroups = cols / group;
-    if (E >= group) {
-        for (int g0 = 0; g0 < E; g0 += group) {
+    if (E >= 16 && group <= 16) {  // a thread holds whole groups (E = 16, group 16): fixed indices
+#pragma unroll
+        for (int g0 = 0; g0 < E; g0 += 16) {
             float ss = 0.f;
-            for (int i = g0; i < g0 + group; ++i) ss += v[i] * v[i];
+#pragma unroll
+            for (int i = g0; i < g0 + 16; ++i) ss += v[i] * v[i];
             const float s = sqrtf(ss * inv_g);
-            scales[row * ngroups + (base + g0) / group] = __half_as_ushort(__float2half_rn(s));
-            for (int i = g0; i < g0 + group; ++i) {
+            scales[row * ngroups + (base + g0) / 16] = __half_as_ushort(__float2half_rn(s));
+#pragma unroll
+            for (int i = g0; i < g0 + 16; ++i) {
                 const float u = s > 0.f ? __fdiv_rn(v[i], s) : 0.f;
                 cd[base + i] = (uint8_t)snap_code(u, thr, nthr);
             }
@@ -379,8 +401,10 @@ __global__ void __launch_bounds__(256, 4) kv_quantize8_kernel(const void* __rest
 // Elements per thread: smallest power of two E with whole warps (dim % 32E == 0),
 // at most 1024 threads, E <= block, and a group spread over at most one warp
 // (group / E <= 32) so the group's sum of squares is a warp-shuffle reduction.
+// Values per thread: the most (up to 16) that still give whole warps, so that more of the
+// transform runs in registers and shuffles and fewer stages go through shared memory.
 int pick_e(int dim, int block, int group) {
-    for (int e = 1; e <= 16; e <<= 1)
+    for (int e = 16; e >= 1; e >>= 1)
         if (e <= block && dim % (32 * e) == 0 && dim / e <= 1024 && group <= 32 * e) return e;
     return 0;
 }
@@ -405,7 +429,7 @@ extern "C" tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int3
     const int e = pick_e(cols, rot->block, group);
     if (e == 0 || cols > 16384) return TQ_ERR_UNSUPPORTED;
     const int threads = cols / e;
-    const size_t smem = (size_t)cols * 4 + 256 * 4 + (size_t)cols;
+    const size_t smem = fwht_pad_floats(cols) * 4 + 256 * 4 + (size_t)cols;
     const float rscale = (float)(1.0 / sqrt((double)rot->block));
     cudaStream_t st = as_stream(stream);
     switch (e) {

@@ -94,7 +94,7 @@ tq_status launch_rotate(const Load& ld, int64_t rows, const tq_rotation_t* rot, 
     if (rows == 0) return TQ_OK;
     if (rows * (dim / span) > 0x7fffffffll) return TQ_ERR_INVALID;
     const int threads = span / e;
-    const size_t smem = (size_t)span * sizeof(float);
+    const size_t smem = fwht_pad_floats(span) * sizeof(float);
     const float scale = (float)(1.0 / sqrt((double)block));
     const dim3 grid((unsigned)(rows * (dim / span)));
     switch (e) {
