@@ -249,6 +249,25 @@ def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
                        "min_pairs_per_expert": int(counts.min())}}
 
 
+def rank_seed(rank):
+    """Seed of a rank's tokens: every replica routes its own tokens (weak scaling)."""
+    return SEED + 17 * rank
+
+
+def max_over_ranks(torch, t_ms, world, dev):
+    """The job's time: the slowest rank's (all-reduce MAX over the process group when world > 1)."""
+    if world <= 1:
+        return t_ms
+    tt = torch.tensor([t_ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_gbs(world, steps, step_bytes, t_ms):
+    """Whole-job throughput: the packed-weight bytes every rank's steps read, over the job's time."""
+    return world * steps * step_bytes / (t_ms * 1e-3) / 1e9
+
+
 def graph_time_us(torch, fn, flush, iters=40, skip=4):
     """Device time (us) of one CUDA-graph replay of fn(), L2 flushed before each replay: the mean
     of the middle 60 % of the replays after warm-up (the event timer ticks in steps of about
@@ -410,8 +429,8 @@ def main():
     rotH = tq.Rotation(HIDDEN, 1024, seed=wl.sign_seed(SEED, 0), device=dev)
     rotI = tq.Rotation(INTER, 2048, seed=wl.sign_seed(SEED, 1), device=dev)
     nsteps = args.warmup + args.steps
-    logits_all = torch.from_numpy(wl.router_logits(SEED + 17 * rank, nsteps, nexp)).to(dev)
-    x_all = torch.from_numpy(wl.activations(SEED + 17 * rank, nsteps, HIDDEN)[0].view("int16")).to(dev).view(
+    logits_all = torch.from_numpy(wl.router_logits(rank_seed(rank), nsteps, nexp)).to(dev)
+    x_all = torch.from_numpy(wl.activations(rank_seed(rank), nsteps, HIDDEN)[0].view("int16")).to(dev).view(
         torch.bfloat16)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     logits_buf = torch.empty((1, nexp), dtype=torch.float32, device=dev)
@@ -490,12 +509,8 @@ def main():
         wall = time.perf_counter() - wall0
     barrier()
     times = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
-    t_ms = sum(times)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_ms = float(tt.item())
-    value = world * args.steps * step_bytes / (t_ms * 1e-3) / 1e9
+    t_ms = max_over_ranks(torch, sum(times), world, dev)
+    value = job_gbs(world, args.steps, step_bytes, t_ms)
     clocks = clk.summary()
 
     # dominant kernel alone: gate||up gather_qmv, one launch per replay, L2 flushed between
@@ -536,8 +551,8 @@ def main():
                 roofline["traffic_capture"] = d["capture"]
 
     # end to end through the Python API: pinned host inputs in, result out, every step
-    h_logits = torch.from_numpy(wl.router_logits(SEED + 17 * rank + 5, nsteps, nexp)).pin_memory()
-    h_x = torch.from_numpy(wl.activations(SEED + 17 * rank + 5, nsteps, HIDDEN)[0].view("int16")).pin_memory()
+    h_logits = torch.from_numpy(wl.router_logits(rank_seed(rank) + 5, nsteps, nexp)).pin_memory()
+    h_x = torch.from_numpy(wl.activations(rank_seed(rank) + 5, nsteps, HIDDEN)[0].view("int16")).pin_memory()
     h_out = torch.empty((nsteps, HIDDEN), dtype=torch.float32).pin_memory()
     d_x = torch.empty((1, HIDDEN), dtype=torch.int16, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -552,12 +567,8 @@ def main():
         h_out[i:i + 1].copy_(out, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+    e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_gbs(world, args.steps, step_bytes, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": nexp * 4 + HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
            "ms_per_step": e2e_ms / args.steps}
 
