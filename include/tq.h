@@ -54,7 +54,7 @@ extern "C" {
 typedef enum tq_status {
     TQ_OK = 0,
     TQ_ERR_INVALID = 1,      /* argument rejected on the host */
-    TQ_ERR_UNSUPPORTED = 2,  /* valid combination that this build does not cover */
+    TQ_ERR_UNSUPPORTED = 2,  /* valid combination that the library does not cover */
     TQ_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     TQ_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (from tq_check_error) */
     TQ_ERR_DEVICE = 5        /* a kernel reported a bad input (from tq_check_error) */
