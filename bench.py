@@ -339,6 +339,12 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
     rec("multi_gather_3bit_T8", graph_time_us(torch, lambda: tq.multi_gather_qmv(qp, hp, pids.view(-1)), flush),
         8 * P_K * per_exp, shape="64 pairs (8 tokens x top-8 of 128) x 4096 x 1536, 3-bit group 64",
         distinct_experts=int(torch.unique(pids).numel()))
+    # dense rotated-domain weights of 8 experts of the same bank, for a regular matmul (bf16 out)
+    dids = torch.tensor([(7 + 13 * j) % P_E for j in range(8)], dtype=torch.int32, device=dev)
+    rec("dequant_experts_3bit_8x4096x1536_bf16",
+        graph_time_us(torch, lambda: tq.dequant_experts(qp, dids, out_dtype=torch.bfloat16), flush),
+        8 * per_exp + 8 * P_H * P_I * 2, shape="8 experts x 4096 x 1536, 3-bit group 64 -> bf16 (codes + scales "
+                                               "read, weights written)")
     del qp
     # KV cache: compress 131072 tokens x 8 heads x 128 (8-bit K, 3-bit V, group 32), then one decode read
     ctx, Hkv, D, KG = 131072, 8, 128, 32
