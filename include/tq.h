@@ -167,7 +167,10 @@ tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int32_t cols, i
  * "How it works", "Running a quantized layer": fused kernels decode the packed
  * codes inline, so the full-precision weights never exist.
  * x_rot: device f32 [T, cols] (already rotated).  y: device [T, rows] of ydt
- * (f32 or bf16).  T >= 1.  cb->levels: 3, 4, 8 or 16. */
+ * (f32 or bf16).  T >= 0 (0: nothing is launched).  cb->levels: 3, 4, 8 or 16.
+ * Arithmetic: fp32 products and sums of the decoded weights (the three-level
+ * kernels hold the input as 16-bit integers with one scale per vector);
+ * tq_qmv_tc is the tensor-core form with fp16 operands. */
 tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T, void* y, tq_dtype ydt, void* stream);
 
 /* MoE decode: every routed expert reads the shared input of its token.
