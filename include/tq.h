@@ -281,9 +281,11 @@ size_t tq_gather_qmm_workspace_bytes(int32_t P, int32_t cols, int32_t per_pair_i
  * scales and must not be shared with a call running concurrently.
  * TQ_ERR_UNSUPPORTED (nothing launched) unless cb->levels is 4, 8 or 16, rows
  * is a multiple of 128, cols a multiple of 64 with at most 64 groups per row,
- * and 1 <= T <= 64; tq_qmv covers the other cases. */
+ * and 1 <= T <= 64; tq_qmv covers the other cases.  err: optional device word
+ * (NULL: not reported); a bounded wait that ran out sets TQ_DEVERR_TIMEOUT
+ * there, and y then holds partial sums. */
 tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_t T, float* y, void* ws, size_t ws_bytes,
-                    void* stream);
+                    uint32_t* err, void* stream);
 size_t tq_qmv_tc_workspace_bytes(int32_t T, int32_t cols);
 
 /* Dequantize selected experts to dense rotated-domain weights, for a regular matmul.
@@ -340,7 +342,9 @@ size_t tq_kv_attend_workspace_bytes(int32_t Hq, int32_t D, int64_t ctx);
  * exits.  No memory is allocated by the call (no cudaMalloc, cudaFree or
  * allocating library routine).  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current) and
- * caches it; make that first call before any stream capture.  Sizes whose
+ * caches it for the device's current CUDA context; make that first call
+ * before any stream capture.  After cudaDeviceReset (a new context) the next
+ * call looks the address up again, so it too belongs before any capture.  Sizes whose
  * scratch, tq_kv_attend_workspace_bytes(Hq, D, ctx), exceeds the maximum
  * return TQ_ERR_INVALID without launching.  All calls on a device share the
  * array, which keeps the previous call's contents (every slot a call reads is

@@ -54,7 +54,7 @@ _SIGS = {
     "tq_quantize": (_i32, [_c_p, _i32, _i64, _i32, _i32, _P(tq_rotation_t), _P(tq_codebook_t), _c_p, _c_p, _i64,
                            _c_p]),
     "tq_qmv": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p]),
-    "tq_qmv_tc": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _sz, _c_p]),
+    "tq_qmv_tc": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _sz, _c_p, _c_p]),
     "tq_qmv_tc_workspace_bytes": (_sz, [_i32, _i32]),
     "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p]),
     "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
@@ -261,7 +261,7 @@ def qmv(w: QWeight, x_rot, out_dtype=None, tensor_cores=True):
     if tensor_cores and y.dtype == torch.float32 and T >= 2:
         nb = int(load().tq_qmv_tc_workspace_bytes(T, w.cols))
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=x_rot.device)
-        st = load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, _stream())
+        st = load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, None, _stream())
         if st != TQ_ERR_UNSUPPORTED:
             _check(st, "tq_qmv_tc")
             return y
@@ -269,7 +269,7 @@ def qmv(w: QWeight, x_rot, out_dtype=None, tensor_cores=True):
     return y
 
 
-def qmv_tc(w: QWeight, x_rot):
+def qmv_tc(w: QWeight, x_rot, err=None):
     """The tensor-core dense matvec alone (raises TQError where it does not apply)."""
     torch = _torch()
     _contig(x_rot, "x_rot")
@@ -278,7 +278,8 @@ def qmv_tc(w: QWeight, x_rot):
     nb = int(load().tq_qmv_tc_workspace_bytes(T, w.cols))
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=x_rot.device)
     q = w.c()
-    _check(load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, _stream()), "tq_qmv_tc")
+    _check(load().tq_qmv_tc(ctypes.byref(q), _ptr(x_rot), T, _ptr(y), _ptr(ws), nb, _ptr(err), _stream()),
+           "tq_qmv_tc")
     return y
 
 

@@ -16,6 +16,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 using namespace tq;
@@ -543,19 +545,51 @@ static __device__ __align__(256) float g_kv_attend_scratch[kNoAllocScratchBytes 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // id of the context the address belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the current CUDA context (0 if the driver cannot say).  A context that
+// cudaDeviceReset destroyed and the runtime re-created gets a new id, so an address cached for
+// the old one is never reused.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        looked = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device.  The host-side
 // name of a __device__ array is only a stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// (with that device current) the first time a device is used in a context and
+// cached; a new context on the device (after cudaDeviceReset) looks it up again.
 tq_status noalloc_scratch(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_kv_attend_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = static_cast<float*>(g_scratch_addr[dev]);
     return TQ_OK;

@@ -1334,7 +1334,7 @@ extern "C" size_t tq_qmv_tc_workspace_bytes(int32_t T, int32_t cols) {
 }
 
 extern "C" tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_t T, float* y, void* ws,
-                               size_t ws_bytes, void* stream) {
+                               size_t ws_bytes, uint32_t* err, void* stream) {
     if (!w || !w->codes || !w->scales || !w->cb.centroids) return TQ_ERR_INVALID;
     if (w->experts <= 0 || w->rows <= 0 || w->cols <= 0) return TQ_ERR_INVALID;
     if (!(w->group == 16 || w->group == 32 || w->group == 64 || w->group == 128) || w->cols % w->group)
@@ -1366,6 +1366,7 @@ extern "C" tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_
     p.y = y;
     p.ydt = TQ_F32;
     p.colscale = cs;
+    p.err = err;
     if (!staged_fits(p, w->group, w->cb.levels)) return TQ_ERR_UNSUPPORTED;
     QmmMaps maps;
     if (!encode_maps(p, x16, maps)) return TQ_ERR_CUDA;

@@ -107,7 +107,7 @@ def test_host_validation_rejects_bad_arguments():
 
 def test_qmv_tc_host_checks_and_workspace():
     """tq_qmv_tc: the shapes it refuses, the workspace rule and the size formula, all decided on the
-    host before any CUDA call."""
+    host before any CUDA call; a NULL error word is accepted (the device simply does not report)."""
     import rotated_codebook_quantized_gb300 as tq
 
     lib = tq.load()
@@ -119,15 +119,15 @@ def test_qmv_tc_host_checks_and_workspace():
     assert need == 3 * 4096 * 2 + 16  # fp16 rows, then 3 row scales in one 16-byte piece
     assert lib.tq_qmv_tc_workspace_bytes(0, 4096) == 0
     ok = tq.tq_qweight_t(fake.value, fake.value, 1, 256, 4096, 128, stride, 0, 0, cb8)
-    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 0, fake, None, 0, None) == tq.TQ_OK  # nothing to do
-    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, -1, fake, fake, need, None) == tq.TQ_ERR_INVALID
-    assert lib.tq_qmv_tc(ctypes.byref(ok), None, 3, fake, fake, need, None) == tq.TQ_ERR_INVALID
-    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 3, fake, fake, need - 16, None) == tq.TQ_ERR_INVALID
-    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 3, fake, ctypes.c_void_p(0x1008), need, None) == tq.TQ_ERR_INVALID
-    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 65, fake, fake, 1 << 30, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 0, fake, None, 0, None, None) == tq.TQ_OK  # nothing to do
+    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, -1, fake, fake, need, None, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_qmv_tc(ctypes.byref(ok), None, 3, fake, fake, need, None, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 3, fake, fake, need - 16, None, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 3, fake, ctypes.c_void_p(0x1008), need, None, None) == tq.TQ_ERR_INVALID
+    assert lib.tq_qmv_tc(ctypes.byref(ok), fake, 65, fake, fake, 1 << 30, None, None) == tq.TQ_ERR_UNSUPPORTED
     tern = tq.tq_qweight_t(fake.value, fake.value, 1, 256, 4096, 128, 208, 0, 0, cb3)
-    assert lib.tq_qmv_tc(ctypes.byref(tern), fake, 3, fake, fake, need, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_qmv_tc(ctypes.byref(tern), fake, 3, fake, fake, need, None, None) == tq.TQ_ERR_UNSUPPORTED
     rows130 = tq.tq_qweight_t(fake.value, fake.value, 1, 130, 4096, 128, stride, 0, 0, cb8)
-    assert lib.tq_qmv_tc(ctypes.byref(rows130), fake, 3, fake, fake, need, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_qmv_tc(ctypes.byref(rows130), fake, 3, fake, fake, need, None, None) == tq.TQ_ERR_UNSUPPORTED
     cols96 = tq.tq_qweight_t(fake.value, fake.value, 1, 256, 96, 32, 12, 0, 0, cb8)
-    assert lib.tq_qmv_tc(ctypes.byref(cols96), fake, 3, fake, fake, need, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_qmv_tc(ctypes.byref(cols96), fake, 3, fake, fake, need, None, None) == tq.TQ_ERR_UNSUPPORTED

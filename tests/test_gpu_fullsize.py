@@ -136,3 +136,107 @@ def test_full_size_dense_qmv_sampled(lib, T):
     assert rel_l2(y32[:, rows].T, ref) < 1e-5
     assert rel_l2(ytc[:, rows].T, ref) < 1e-3
     assert rel_l2(lib.qmv(qw, xd).cpu().numpy()[:, rows].T, ref) < REL_L2  # the form qmv() picks at this T
+
+
+def _bit_bank_experts(lib, experts, rows, cols, levels, group, seed):
+    """Random valid bit-packed words and fp16 scales of an expert bank, drawn on the device."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    b = {4: 2, 8: 3, 16: 4}[levels]
+    cw = o.codes_per_word(levels)
+    nw = -(-cols // cw)
+    stride = lib.row_stride_words(levels, cols)
+    codes = torch.zeros((experts, rows, stride), dtype=torch.int32, device="cuda")
+    for e0 in range(0, experts, 16):
+        n = min(16, experts - e0)
+        w = torch.randint(0, 1 << (b * cw), (n, rows, nw), generator=g, device="cuda", dtype=torch.int64)
+        w[..., -1] &= (1 << (b * (cols - (nw - 1) * cw))) - 1
+        codes[e0:e0 + n, :, :nw] = (w - (w >= 2 ** 31).long() * 2 ** 32).to(torch.int32)
+    sc = (torch.exp(torch.randn((experts, rows, cols // group), generator=g, device="cuda") * 0.5 - 3.5)).half()
+    return codes, sc
+
+
+def test_full_size_prefill_gather_qmm_sampled(lib):
+    """MoE prefill at full size in the benchmark's launch configuration: 4096 tokens routed top-8
+    of 128 experts (N(0,1) + Zipf(1.1) logits), gate||up 3072 x 4096 and per-pair down 4096 x 1536,
+    3-bit group 64, fp16 operands.  32 sampled outputs from each of the hottest, the median and the
+    coldest expert of each projection (96 per projection) against the oracle's decode of those rows."""
+    PE, PT, PK, PH, PI, PG, L = 128, 4096, 8, 4096, 1536, 64, 8
+    rs = np.random.default_rng(20261203)
+    oc, _ = o.lloyd_max_gaussian(L)
+    cb = lib.Codebook(L)
+    gu_codes, gu_sc = _bit_bank_experts(lib, PE, 2 * PI, PH, L, PG, 1301)
+    dn_codes, dn_sc = _bit_bank_experts(lib, PE, PH, PI, L, PG, 1302)
+    qgu = lib.QWeight(gu_codes, gu_sc.view(torch.int16), PE, 2 * PI, PH, PG, cb, row_stride=gu_codes.shape[-1])
+    qdn = lib.QWeight(dn_codes, dn_sc.view(torch.int16), PE, PH, PI, PG, cb, row_stride=dn_codes.shape[-1])
+    logits = wl.router_logits(wl.SEED_MOE_PREFILL, PT, PE, zipf=1.1)
+    _, _, perm, _, off = lib.moe_route(torch.from_numpy(logits).cuda(), PK)
+    oids, _ = o.route(logits, PK)
+    operm, ooff = o.sort_pairs(oids, PE)
+    np.testing.assert_array_equal(perm.cpu().numpy(), operm)
+    np.testing.assert_array_equal(off.cpu().numpy(), ooff)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1303)
+    x = torch.randn((PT, PH), generator=g, device="cuda").half()
+    h = torch.randn((PT * PK, PI), generator=g, device="cuda").half()
+    ygu = lib.gather_qmm(qgu, x, perm, off, PK).cpu().numpy()
+    ydn = lib.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True).cpu().numpy()
+    counts = np.diff(ooff)
+    order = [e for e in np.argsort(-counts, kind="stable") if counts[e] > 0]
+    picks = [order[0], order[len(order) // 2], order[-1]]  # hottest, median, coldest routed expert
+    assert counts[picks[0]] > 1000 and counts[picks[2]] < counts[picks[0]]
+    xh = x.cpu().numpy().astype(np.float64)
+    hh = h.cpu().numpy().astype(np.float64)
+    for codes, sc, y, rows, K, inp, by_token in ((gu_codes, gu_sc, ygu, 2 * PI, PH, xh, True),
+                                                 (dn_codes, dn_sc, ydn, PH, PI, hh, False)):
+        got, ref = [], []
+        for e in picks:
+            lo, hi = int(ooff[e]), int(ooff[e + 1])
+            pos = rs.integers(lo, hi, 32)
+            rws = rs.integers(0, rows, 32)
+            W = _rows(codes, sc, int(e), rws, L, K, PG, oc)  # [32, K]
+            for i, (ps, r) in enumerate(zip(pos, rws)):
+                src = inp[int(operm[ps]) // PK] if by_token else inp[int(ps)]
+                ref.append(float(W[i] @ src))
+                got.append(float(y[ps, r]))
+        assert rel_l2(np.array(got), np.array(ref)) < REL_L2
+
+
+def test_full_size_kv_attend_sampled(lib):
+    """KV decode read at full size: 131072 cached tokens x 8 kv heads x 128 (8-bit keys, 3-bit values,
+    group 32), 32 query heads, 128 split-context partials merged.  The cache is random valid codes
+    and fp16 scales drawn on the device; the oracle dequantizes kv heads 2 and 7, de-rotates, and
+    runs softmax attention for the 8 query heads that read them."""
+    ctx, Hkv, D, Hq, KG = 131072, 8, 128, 32, 32
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1401)
+    signs = o.rotation_signs(wl.sign_seed(wl.SEED_KV, 0), D)
+    rot = lib.Rotation(D, D, signs=signs)
+    cache = lib.KVCache(ctx, Hkv, D, KG, lib.Codebook(256), lib.Codebook(8), rot)
+    kw = cache.kw
+    k_words = torch.randint(0, 2 ** 32, (Hkv, ctx, kw), generator=g, device="cuda", dtype=torch.int64)
+    cache.kcodes.copy_((k_words - (k_words >= 2 ** 31).long() * 2 ** 32).to(torch.int32))
+    del k_words
+    v_words = torch.randint(0, 2 ** 30, (Hkv, ctx, cache.vw), generator=g, device="cuda", dtype=torch.int64)
+    v_words[..., -1] &= (1 << (3 * (D - (cache.vw - 1) * 10))) - 1
+    cache.vcodes.copy_(v_words.to(torch.int32))
+    del v_words
+    cache.kscales.copy_(torch.exp(torch.randn((Hkv, ctx, D // KG), generator=g, device="cuda") * 0.5).half()
+                        .view(torch.int16))
+    cache.vscales.copy_(torch.exp(torch.randn((Hkv, ctx, D // KG), generator=g, device="cuda") * 0.5).half()
+                        .view(torch.int16))
+    cache.length = ctx
+    qb, q = wl.kv_query()
+    qd = torch.from_numpy(np.ascontiguousarray(qb).view(np.int16)).cuda().view(torch.bfloat16)
+    out = lib.kv_attend(cache, qd).cpu().numpy()
+    kc, _ = o.lloyd_max_gaussian(256)
+    vc, _ = o.lloyd_max_gaussian(8)
+    grp = Hq // Hkv
+    for kvh in (2, 7):
+        Kh = o.dequantize(o.unpack(cache.kcodes[kvh].cpu().numpy().view(np.uint32), 256, D),
+                          cache.kscales[kvh].cpu().numpy().view(np.float16), kc, KG)
+        Vh = o.dequantize(o.unpack(cache.vcodes[kvh].cpu().numpy().view(np.uint32), 8, D),
+                          cache.vscales[kvh].cpu().numpy().view(np.float16), vc, KG)
+        heads = list(range(kvh * grp, (kvh + 1) * grp))
+        ref = o.kv_attend(q[heads], Kh[None], Vh[None], signs)
+        assert rel_l2(out[heads], ref) < REL_L2, kvh
