@@ -178,17 +178,30 @@ tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T, void* y, 
  * (polar_gather_qmv).  y[t, j, :] = W_{ids[t, j]} x_rot[t].
  * x_rot: device f32 [T, cols].  ids: device int32 [T, k].  y: device
  * [T, k, rows] of ydt (f32 or bf16).  Out-of-range ids zero their row of y
- * and set TQ_DEVERR_BAD_ID in *err. */
+ * and set TQ_DEVERR_BAD_ID in *err.
+ * ws: 16-byte aligned device scratch of tq_gather_qmv_workspace_bytes(w, T, k)
+ * bytes, or NULL.  Three-level books with group 16 run a table-lookup kernel
+ * that splits rows wider than 2560 columns among CTAs; their partial sums go
+ * to ws.  With ws NULL (or too small) such rows take the single-pass kernel
+ * instead (slower); a size of 0 means no scratch is needed.
+ * Arithmetic of the three-level kernels: the input is held as integers per
+ * group of 16 columns (|xq| <= 8191, one fp32 scale per group; the
+ * single-pass kernel: 16-bit, one scale per vector); products and sums of
+ * those integers are exact, the group and weight scales are applied in fp32.
+ * Bit-packed books: fp32 products and sums. */
 tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
-                        void* y, tq_dtype ydt, uint32_t* err, void* stream);
+                        void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
+size_t tq_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t T, int32_t k);
 
 /* MoE with a different input for each (expert, input) pair.
  * "How it works", row "Prefill with a different input per expert"
  * (polar_multi_gather_qmv).  y[p, :] = W_{ids[p]} x_rot[p].
  * x_rot: device f32 [P, cols].  ids: device int32 [P].  y: device [P, rows]
- * of ydt (f32 or bf16). */
+ * of ydt (f32 or bf16).  ws / ws_bytes and the arithmetic as for
+ * tq_gather_qmv (tq_multi_gather_qmv_workspace_bytes(w, P) bytes). */
 tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
-                              void* y, tq_dtype ydt, uint32_t* err, void* stream);
+                              void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
+size_t tq_multi_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t P);
 
 /* tq_gather_qmv with the input rotation done inside the matvec: y[t, j, :] =
  * W_{ids[t, j]} (R x[t]), R = rot (blockdiag(H_block) diag(signs) / sqrt(block),

@@ -56,8 +56,10 @@ _SIGS = {
     "tq_qmv": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _i32, _c_p]),
     "tq_qmv_tc": (_i32, [_P(tq_qweight_t), _c_p, _i32, _c_p, _c_p, _sz, _c_p, _c_p]),
     "tq_qmv_tc_workspace_bytes": (_sz, [_i32, _i32]),
-    "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p]),
-    "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _c_p]),
+    "tq_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _i32, _c_p, _i32, _c_p, _sz, _c_p, _c_p]),
+    "tq_gather_qmv_workspace_bytes": (_sz, [_P(tq_qweight_t), _i32, _i32]),
+    "tq_multi_gather_qmv": (_i32, [_P(tq_qweight_t), _c_p, _c_p, _i32, _c_p, _i32, _c_p, _sz, _c_p, _c_p]),
+    "tq_multi_gather_qmv_workspace_bytes": (_sz, [_P(tq_qweight_t), _i32]),
     "tq_gather_qmv_rotate": (_i32, [_P(tq_qweight_t), _c_p, _i32, _P(tq_rotation_t), _c_p, _i32, _i32, _c_p, _i32,
                                     _c_p, _c_p]),
     "tq_multi_gather_qmv_swiglu": (_i32, [_P(tq_qweight_t), _c_p, _P(tq_rotation_t), _c_p, _i32, _c_p, _i32, _c_p,
@@ -283,27 +285,43 @@ def qmv_tc(w: QWeight, x_rot, err=None):
     return y
 
 
-def gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
+def _workspace(nbytes: int, device, ws=None):
+    """A caller's scratch buffer if it is large enough, else a new one (None when nothing is needed)."""
+    if nbytes <= 0:
+        return None
+    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+        return ws
+    return _torch().empty(nbytes, dtype=_torch().uint8, device=device)
+
+
+def gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None, ws=None, use_ws=True):
+    """y[t, j] = W_{ids[t, j]} x_rot[t].  use_ws=False passes no scratch (the single-pass kernel
+    then takes rows the table-lookup kernel would split)."""
     torch = _torch()
     _contig(x_rot, "x_rot")
     _contig(ids, "ids")
     T, k = ids.shape
     y = torch.empty((T, k, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
     q = w.c()
-    _check(load().tq_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), T, k, _ptr(y), _dt(y), _ptr(err), _stream()),
-           "tq_gather_qmv")
+    nb = int(load().tq_gather_qmv_workspace_bytes(ctypes.byref(q), T, k)) if use_ws else 0
+    ws = _workspace(nb, x_rot.device, ws)
+    _check(load().tq_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), T, k, _ptr(y), _dt(y), _ptr(ws), nb,
+                                _ptr(err), _stream()), "tq_gather_qmv")
     return y
 
 
-def multi_gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None):
+def multi_gather_qmv(w: QWeight, x_rot, ids, out_dtype=None, err=None, ws=None, use_ws=True):
+    """y[p] = W_{ids[p]} x_rot[p] (use_ws as for gather_qmv)."""
     torch = _torch()
     _contig(x_rot, "x_rot")
     _contig(ids, "ids")
     P = ids.shape[0]
     y = torch.empty((P, w.rows), dtype=out_dtype or torch.float32, device=x_rot.device)
     q = w.c()
-    _check(load().tq_multi_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), P, _ptr(y), _dt(y), _ptr(err),
-                                      _stream()), "tq_multi_gather_qmv")
+    nb = int(load().tq_multi_gather_qmv_workspace_bytes(ctypes.byref(q), P)) if use_ws else 0
+    ws = _workspace(nb, x_rot.device, ws)
+    _check(load().tq_multi_gather_qmv(ctypes.byref(q), _ptr(x_rot), _ptr(ids), P, _ptr(y), _dt(y), _ptr(ws), nb,
+                                      _ptr(err), _stream()), "tq_multi_gather_qmv")
     return y
 
 

@@ -108,8 +108,37 @@ extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T
     return run(p, w->group, nv, (T + nv - 1) / nv, as_stream(stream));
 }
 
+namespace {
+
+// The table-lookup kernel when it applies and its scratch is there; else the single-pass kernels.
+tq_status run_items(const QmvParams& p, int group, int n_items, void* ws, size_t ws_bytes, cudaStream_t st) {
+    if (qmv_lut_ok(p, group)) {
+        const size_t need = qmv_lut_workspace_bytes(p.cols, n_items, p.rows);
+        if (need == 0 || (ws && ws_bytes >= need && aligned(ws, 16))) {
+            const tq_status s = qmv_lut_run(p, n_items, ws, ws_bytes, st);
+            if (s != TQ_ERR_UNSUPPORTED) return s;
+        }
+    }
+    return run(p, group, 1, n_items, st);
+}
+
+size_t items_workspace(const tq_qweight_t* w, int64_t n_items) {
+    if (!w || w->cb.levels != 3 || w->group != 16 || w->rows <= 0 || w->cols <= 0 || n_items <= 0) return 0;
+    return qmv_lut_workspace_bytes(w->cols, n_items, w->rows);
+}
+
+}  // namespace
+
+extern "C" size_t tq_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t T, int32_t k) {
+    return T > 0 && k > 0 ? items_workspace(w, (int64_t)T * k) : 0;
+}
+
+extern "C" size_t tq_multi_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t P) {
+    return items_workspace(w, P);
+}
+
 extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
-                                   void* y, tq_dtype ydt, uint32_t* err, void* stream) {
+                                   void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream) {
     tq_status s = check_qweight(w);
     if (s != TQ_OK) return s;
     if (T < 0 || k <= 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
@@ -121,11 +150,12 @@ extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, co
     p.mode = kModeGather;
     p.ids = ids;
     p.k = k;
-    return run(p, w->group, 1, T * k, as_stream(stream));
+    return run_items(p, w->group, T * k, ws, ws_bytes, as_stream(stream));
 }
 
 extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
-                                         void* y, tq_dtype ydt, uint32_t* err, void* stream) {
+                                         void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err,
+                                         void* stream) {
     tq_status s = check_qweight(w);
     if (s != TQ_OK) return s;
     if (P < 0 || !ydt_ok(ydt)) return TQ_ERR_INVALID;
@@ -136,7 +166,7 @@ extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_r
     p.mode = kModeMulti;
     p.ids = ids;
     p.k = 1;
-    return run(p, w->group, 1, P, as_stream(stream));
+    return run_items(p, w->group, P, ws, ws_bytes, as_stream(stream));
 }
 
 extern "C" tq_status tq_gather_qmv_rotate(const tq_qweight_t* w, const void* x, tq_dtype xdt,

@@ -302,6 +302,11 @@ tq_status qmv_trit_run(const QmvParams& p, int group, int n_items, cudaStream_t 
 // where that kernel does not apply.
 tq_status qmv_trit_xstage_run(const QmvParams& p, int group, int n_items, int xmode, const void* xin, int xdt,
                               const int8_t* signs, int block, cudaStream_t st);
+// Ternary books by table lookup (qmv_lut.cu): gather and multi modes.  Rows wider than one
+// column slice need qmv_lut_workspace_bytes of scratch for the slices' partial sums.
+bool qmv_lut_ok(const QmvParams& p, int group);
+size_t qmv_lut_workspace_bytes(int cols, int64_t n_items, int rows);
+tq_status qmv_lut_run(const QmvParams& p, int n_items, void* ws, size_t ws_bytes, cudaStream_t st);
 bool qmv_bits_ok(const QmvParams& p, int group);
 tq_status qmv_bits_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
 

@@ -114,7 +114,7 @@ def test_multi_gather_qmv_bitpacked(lib, levels, group, K, rows):
 
 
 def test_multi_gather_qmv_ternary_repeats_and_bad_id(lib):
-    """Ternary book, per-pair inputs with repeated experts and a bad id (16-bit input: 1e-4)."""
+    """Ternary book, per-pair inputs with repeated experts and a bad id (integer input per group: 2.5e-4)."""
     E, rows, K, group = 10, 96, 2048, 16
     qw, Wh = _bank(lib, 3, E, rows, K, group, seed=77)
     ids = np.array([4, 4, 9, 0, 4, 2, 9, 7], dtype=np.int32)
@@ -127,7 +127,7 @@ def test_multi_gather_qmv_ternary_repeats_and_bad_id(lib):
     assert lib.check_error(err) == lib.TQ_DEVERR_BAD_ID
     assert np.all(y[2] == 0)
     keep = np.arange(len(ids)) != 2
-    assert rel_l2(y[keep], ref[keep]) < 1e-4
+    assert rel_l2(y[keep], ref[keep]) < 2.5e-4
 
 
 def _qmm_random(lib, levels, group, E, rows, K, T, k, seed, zipf=1.1):

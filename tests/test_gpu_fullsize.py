@@ -22,9 +22,10 @@ torch = pytest.importorskip("torch")
 E, TOPK, H, I, G = 384, 8, 7168, 2048, 16
 SAMPLES = 96
 
-# The ternary kernel holds the input as 16-bit integers with one scale per vector: about
-# 4e-5 relative error per dot product (rms); a sample of 96 outputs stays under 2e-4.
-TRIT_TOL = 2e-4
+# The ternary table-lookup kernel holds the input as integers per group of 16 columns
+# (|xq| <= 8191): about 7e-5 relative error per dot product (rms) for Gaussian inputs; a
+# sample of 96 outputs stays under 2.5e-4.
+TRIT_TOL = 2.5e-4
 
 
 def _trit_bank(lib, experts, rows, cols, seed):

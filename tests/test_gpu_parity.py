@@ -136,9 +136,11 @@ def test_quantize_then_qmv(lib, levels, group, K, block, rows, wdt, T):
 
 def _decode_tol(levels):
     """Decode-only tolerance.  Bit-packed books: fp32 arithmetic only (1e-5).  The
-    ternary kernel holds the input as 16-bit integers per group (error <= max|x|/65534
-    per element, at most sqrt(G) times the group RMS: about 3.5e-5 relative), so 1e-4."""
-    return 1e-4 if levels == 3 else 1e-5
+    three-level table-lookup kernel holds the input as integers per group of 16 columns,
+    |xq| <= 8191 (rounding error uniform in +-max_g/16382 per element: for Gaussian inputs
+    about 7e-5 of the output's RMS); the single-pass kernel as 16-bit integers per vector
+    (about 4e-5).  Bar: 2.5e-4."""
+    return 2.5e-4 if levels == 3 else 1e-5
 
 
 def _random_bank(levels, experts, rows, K, group, seed):
@@ -253,6 +255,10 @@ def test_gather_qmv_and_bad_ids(lib):
     y = lib.gather_qmv(qw, _dev(x), _dev(ids), err=err).cpu().numpy()
     ref = o.gather_qmv(Wh, ids, x)
     assert rel_l2(y, ref) < _decode_tol(3)
+    assert lib.check_error(err) == 0
+    # without scratch the single-pass kernel takes the 7168-wide rows
+    y1 = lib.gather_qmv(qw, _dev(x), _dev(ids), err=err, use_ws=False).cpu().numpy()
+    assert rel_l2(y1, ref) < _decode_tol(3)
     assert lib.check_error(err) == 0
     bad = ids.copy()
     bad[1, 2] = 12
@@ -383,7 +389,7 @@ def test_moe_decode_fused_stages(lib, E, k, H, I):
     ids, probs, _, _, _ = lib.moe_route(_dev(logits), k)
     gu_f = lib.gather_qmv_rotate(qgu, _dev(x), rotH, ids)
     gu_s = lib.gather_qmv(qgu, lib.rotate(_dev(x), rotH), ids)
-    assert rel_l2(gu_f.cpu().numpy(), gu_s.cpu().numpy()) < 1e-4
+    assert rel_l2(gu_f.cpu().numpy(), gu_s.cpu().numpy()) < 2.5e-4  # two integer input forms (see _decode_tol)
     gu_b = lib.gather_qmv_rotate(qgu, _bf16_dev(xb), rotH, ids)  # bf16 input, the same values
     assert rel_l2(gu_b.cpu().numpy(), gu_f.cpu().numpy()) < 1e-6
     yd = lib.multi_gather_qmv_swiglu(qdn, gu_f.reshape(k, 2 * I), rotI, ids.reshape(-1))
