@@ -3,21 +3,21 @@
 Workload: one MoE decode step = route 1 token over 384 experts (top-8, fp32
 logits), rotate its bf16 [1, 7168] input, gate||up gather-qmv over the 8
 routed ternary experts (group 16, 20 trits per word), SwiGLU + rotation of the
-2048-wide intermediate, down multi-gather-qmv, router-weighted combine (six
-launches, routing and the input rotation side by side on two streams; the
-same six in one stream, and the forms with the SwiGLU, or also the input
-rotation, inside the matvec are timed beside it as step_variants).  The metric
-is packed-weight bytes read per second by the step (codes + fp16 scales of the
-8 routed experts, 114,720,768 B per step).
+2048-wide intermediate, down multi-gather-qmv, router-weighted combine.  The
+metric is packed-weight bytes read per second by the step (codes + fp16 scales
+of the 8 routed experts, 114,720,768 B per step).
 
-Timing: inputs resident in HBM; each timed step is one CUDA-graph replay of the
-whole step between two CUDA events, with a 256 MiB L2 flush before every step
-(outside the events) and a 5.5 GB expert bank, so every step reads its experts
-from HBM.  ``e2e`` repeats the step (eagerly, in one stream) through the Python API with the step's
-inputs copied from pinned host memory and its output copied back.
-
-Also measured: the gate||up gather-qmv launch alone (roofline of the dominant
-kernel), and the fp64 oracle on a bounded sample on the host cores.
+Timing: inputs resident in HBM.  The K timed steps are one CUDA-graph replay
+of K consecutive steps, step i routing its own token afresh over a 5.5 GB
+expert bank (inputs far larger than L2, so no flush is needed: consecutive
+steps share about 2 % of their experts), between two CUDA events; W warm-up
+steps on other tokens run before, in a graph of their own.  The dominant kernel
+(the gate||up gather) is timed the same way: 32 calls on 32 fresh routings in
+one graph.  ``step_isolated_us`` also reports one step replayed alone after a
+256 MiB L2 flush (that method's event-to-event floor, about 6.7 us for an empty
+graph, is part of it).  ``e2e`` repeats the step through the Python API with
+the step's inputs copied from pinned host memory and its output copied back.
+The fp64 oracle is timed on a bounded sample on the host cores.
 """
 from __future__ import annotations
 
@@ -34,6 +34,9 @@ sys.path.insert(0, ROOT)
 
 E, TOPK, HIDDEN, INTER, GROUP = 384, 8, 7168, 2048, 16
 SEED = 3
+# the arithmetic of the dominant kernel: the rotated input as integers per group of 16 (|xq| <= 8191)
+# times the trits, summed exactly in int32 from a 16-bit table; group and weight scales applied in fp32
+DTYPE = "int14 x trit -> int32, fp32 scales"
 
 
 def packed_bytes_per_expert():
@@ -56,7 +59,7 @@ def measured_peaks():
 
 # ---------------------------------------------------------------- oracle on the host
 
-def oracle_sample(seconds: float, rows_per_expert: int = 48):
+def oracle_sample(seconds: float, rows_per_expert: int = 48, seed_offset: int = 0):
     """Time the fp64 oracle's decode-matvec on sampled rows of routed experts.
 
     Returns (bytes processed, seconds, description).  Runs single-threaded
@@ -67,7 +70,7 @@ def oracle_sample(seconds: float, rows_per_expert: int = 48):
     from rotated_codebook_quantized_gb300 import workloads as wl
 
     c3, _ = o.lloyd_max_gaussian(3)
-    g = wl.rng(SEED, 77)
+    g = wl.rng(SEED, 77, seed_offset)
     _, x = wl.activations(SEED, 1, HIDDEN)
     signs = o.rotation_signs(wl.sign_seed(SEED, 0), HIDDEN)
     xr = o.rotate(x, signs, o.rotation_block(HIDDEN))[0]
@@ -93,15 +96,75 @@ def oracle_sample(seconds: float, rows_per_expert: int = 48):
     return done_bytes, dt, desc
 
 
+_BARRIER = None
+
+
+def _oracle_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+
+
+def _oracle_worker(args):
+    seconds, idx = args
+    oracle_sample(0.0, seed_offset=idx)  # imports and first-call costs outside the timed window
+    _BARRIER.wait()
+    b, s, _ = oracle_sample(seconds, seed_offset=idx)
+    return b, s
+
+
+def oracle_sample_parallel(seconds: float, procs: int):
+    """The same oracle sample on `procs` processes at once (spawned, one numpy thread each, started
+    together after a barrier): (total bytes per second summed over the processes, seconds)."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    with ctx.Pool(procs, initializer=_oracle_init, initargs=(barrier,)) as pool:
+        res = pool.map(_oracle_worker, [(seconds, i) for i in range(procs)])
+    rate = sum(b / s for b, s in res)
+    return rate, max(s for _, s in res)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline_subprocess(seconds: float):
+    """The oracle timed on one host core, then on all of them (a subprocess, before this process touches
+    the GPU)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(seconds)],
                        capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "oracle sample failed"}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": d["desc"]}
+    out = {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": d["desc"], "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+    procs = os.cpu_count() or 1
+    if procs > 1:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(seconds / 2),
+                            "--_oracle-procs", str(procs)], capture_output=True, text=True, env=env, cwd=ROOT)
+        if r.returncode == 0:
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            out["all_cores"] = {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": procs,
+                                "sample": f"the same sample on {procs} processes at once (one numpy thread each)"}
+    return out
 
 
 # ---------------------------------------------------------------- clocks
@@ -208,8 +271,9 @@ def random_bit_bank(torch, tq, dev, gen, experts, rows, cols, levels, group):
     return tq.QWeight(codes, sc.view(torch.int16), experts, rows, cols, group, cb, row_stride=stride)
 
 
-def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
-    """gate||up and down gather_qmm over 4096 tokens routed top-8 of 128 experts (Zipf-skewed)."""
+def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=4):
+    """gate||up and down gather_qmm over 4096 tokens routed top-8 of 128 experts (Zipf-skewed); each
+    projection reads 1 GB of weights per call, so calls run back to back in one CUDA graph."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + P_SEED)
     qgu = random_bit_bank(torch, tq, dev, gen, P_E, 2 * P_I, P_H, 8, P_G)
@@ -219,21 +283,9 @@ def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
     x = torch.randn((P_T, P_H), generator=gen, device=dev).half()
     h = torch.randn((P_T * P_K, P_I), generator=gen, device=dev).half()
     P = P_T * P_K
-    for _ in range(2):
-        tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)
-        tq.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True, out_dtype=torch.bfloat16)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
-    for i in range(iters):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record()
-        tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)
-        ev[i][1].record()
-        tq.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True, out_dtype=torch.bfloat16)
-        ev[i][2].record()
-    torch.cuda.synchronize()
-    t_gu = sorted(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))[iters // 2]
-    t_dn = sorted(ev[i][1].elapsed_time(ev[i][2]) for i in range(iters))[iters // 2]
+    t_gu = b2b_graph_us(torch, [lambda: tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)] * iters) * 1e-3
+    t_dn = b2b_graph_us(torch, [lambda: tq.gather_qmm(qdn, h, perm, off, 1, per_pair_input=True,
+                                                      out_dtype=torch.bfloat16)] * iters) * 1e-3
     f_gu = 2.0 * P * (2 * P_I) * P_H
     f_dn = 2.0 * P * P_H * P_I
     tf = (f_gu + f_dn) / ((t_gu + t_dn) * 1e-3) / 1e12
@@ -243,6 +295,7 @@ def measure_prefill(torch, tq, wl, dev, flush, peaks, iters=10):
             "peak_source": peaks["source"] + " (bf16 burst; fp16 operands have the same dense rate)",
             "flops_per_step": f_gu + f_dn, "ms_gate_up": t_gu, "ms_down": t_dn,
             "tflops_gate_up": f_gu / (t_gu * 1e-3) / 1e12, "tflops_down": f_dn / (t_dn * 1e-3) / 1e12,
+            "timing": "calls back to back in one CUDA graph (1 GB of weights per call)",
             "config": {"tokens": P_T, "experts": P_E, "top_k": P_K, "hidden": P_H, "intermediate": P_I,
                        "bits": 3, "group": P_G, "operands": "fp16", "output": "bf16",
                        "router": "N(0,1) + Zipf(1.1) bias", "max_pairs_per_expert": int(counts.max()),
@@ -295,11 +348,41 @@ def graph_time_us(torch, fn, flush, iters=40, skip=4):
     return sum(mid) / len(mid) * 1e3
 
 
+def b2b_graph_us(torch, fns, reps=3):
+    """Device time (us) per call of the calls fns[0](), fns[1](), ... captured back to back in one CUDA
+    graph (each call on its own inputs, so that together they exceed L2): the best of `reps`
+    replays, divided by the number of calls."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for f in fns[:2]:
+        f()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for f in fns:
+                f()
+    torch.cuda.current_stream().wait_stream(st)
+    g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e3 / len(fns))
+    return best
+
+
 def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
-    """The other hot-path calls at the pages' workload shapes, each timed alone (HBM-bound: GB/s and
-    fraction of the measured copy peak).  Algorithmic bytes: unpadded code words + fp16 scales of
-    the matrices a call reads (per pair for multi_gather), KV codes + scales for attention, inputs
-    read + codes and scales written for the encoders."""
+    """The other hot-path calls at the pages' workload shapes, each timed back to back in one CUDA
+    graph on inputs that together exceed L2 (HBM-bound: GB/s and fraction of the measured copy peak).
+    Algorithmic bytes: unpadded code words + fp16 scales of the matrices a call reads (each distinct
+    expert once), KV codes + scales for attention, inputs read + codes and scales written for the
+    encoders, weights written for dequant_experts."""
     hbm = peaks["hbm_gbs"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000)
@@ -309,40 +392,45 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
         gbs = nbytes / (us * 1e-6) / 1e9
         out[name] = dict(us=us, bytes=nbytes, gbs=gbs, frac_of_hbm_peak=gbs / hbm, **kw)
 
-    # dense 3-bit qmv, 11008 x 4096, group 128, T in {1, 4, 16}
+    # dense 3-bit qmv, 11008 x 4096, group 128, T in {1, 4, 16}: 8 copies of the matrix (150 MB) in turn
     N, K, G = 11008, 4096, 128
-    qd = random_bit_bank(torch, tq, dev, gen, 1, N, K, 8, G)
+    qds = [random_bit_bank(torch, tq, dev, gen, 1, N, K, 8, G) for _ in range(8)]
     wbytes = N * (tq.row_words(8, K) * 4 + (K // G) * 2)
     for T in (1, 4, 16):
         x = torch.randn((T, K), generator=gen, device=dev)
-        rec(f"dense_qmv_3bit_T{T}", graph_time_us(torch, lambda: tq.qmv(qd, x), flush), wbytes,
+        rec(f"dense_qmv_3bit_T{T}", b2b_graph_us(torch, [lambda q=q: tq.qmv(q, x) for q in qds] * 2), wbytes,
             shape="11008 x 4096, 3-bit, group 128")
-    # encode (rotate, group RMS, snap, pack) of the same matrix from bf16
-    Wb = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    del qds
+    # encode (rotate, group RMS, snap, pack) of the same matrix from bf16: two inputs in turn (180 MB)
+    Wbs = [(torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16) for _ in range(2)]
     rot = tq.Rotation(K, 4096, seed=11, device=dev)
     cb8 = tq.Codebook(8, device=dev)
-    rec("quantize_3bit_11008x4096", graph_time_us(torch, lambda: tq.quantize(Wb, G, rot, cb8), flush),
+    rec("quantize_3bit_11008x4096", b2b_graph_us(torch, [lambda w=w: tq.quantize(w, G, rot, cb8) for w in Wbs] * 4),
         N * K * 2 + wbytes, shape="bf16 in, 3-bit codes + fp16 scales out")
-    del Wb
-    # decode down projection alone: multi_gather_qmv over the 8 routed ternary experts
-    ids = torch.tensor([(5 + 41 * j) % qdn.experts for j in range(TOPK)], dtype=torch.int32, device=dev)
+    del Wbs
+    # decode down projection alone: multi_gather_qmv over 8 routed ternary experts, fresh routing per call
+    dlog = torch.from_numpy(wl.router_logits(SEED + 23, 16, qdn.experts)).to(dev)
+    dids = [tq.moe_route(dlog[i:i + 1], TOPK, sort=False)[0].view(-1) for i in range(16)]
     h = torch.randn((TOPK, INTER), generator=gen, device=dev)
     _, dn_b = packed_bytes_per_expert()
-    rec("decode_down_multi_gather_ternary", graph_time_us(torch, lambda: tq.multi_gather_qmv(qdn, h, ids), flush),
+    rec("decode_down_multi_gather_ternary", b2b_graph_us(torch, [lambda i=i: tq.multi_gather_qmv(qdn, h, dids[i])
+                                                                 for i in range(16)]),
         TOPK * dn_b, shape="8 experts x 7168 x 2048, ternary group 16")
     # per-pair inputs at T = 8 (prefill-shaped down projection): 64 pairs over 128 experts, 3-bit group 64
     qp = random_bit_bank(torch, tq, dev, gen, P_E, P_H, P_I, 8, P_G)
-    logits = torch.from_numpy(wl.router_logits(P_SEED, 8, P_E, zipf=1.1)).to(dev)
-    pids, _, _, _, _ = tq.moe_route(logits, P_K, sort=False)
-    hp = torch.randn((8 * P_K, P_I), generator=gen, device=dev)
     per_exp = P_H * (tq.row_words(8, P_I) * 4 + (P_I // P_G) * 2)
-    rec("multi_gather_3bit_T8", graph_time_us(torch, lambda: tq.multi_gather_qmv(qp, hp, pids.view(-1)), flush),
-        8 * P_K * per_exp, shape="64 pairs (8 tokens x top-8 of 128) x 4096 x 1536, 3-bit group 64",
-        distinct_experts=int(torch.unique(pids).numel()))
+    plog = torch.from_numpy(wl.router_logits(P_SEED, 8 * 8, P_E, zipf=1.1)).to(dev)
+    pids = [tq.moe_route(plog[8 * i:8 * i + 8], P_K, sort=False)[0].view(-1) for i in range(8)]
+    hp = torch.randn((8 * P_K, P_I), generator=gen, device=dev)
+    distinct = sum(int(torch.unique(p).numel()) for p in pids) / len(pids)
+    rec("multi_gather_3bit_T8", b2b_graph_us(torch, [lambda p=p: tq.multi_gather_qmv(qp, hp, p) for p in pids] * 2),
+        distinct * per_exp, shape="64 pairs (8 tokens x top-8 of 128) x 4096 x 1536, 3-bit group 64",
+        distinct_experts=distinct, bytes_counted="distinct experts x bytes per expert (each read once)")
     # dense rotated-domain weights of 8 experts of the same bank, for a regular matmul (bf16 out)
-    dids = torch.tensor([(7 + 13 * j) % P_E for j in range(8)], dtype=torch.int32, device=dev)
+    qids = [torch.tensor([(7 + 13 * j + 8 * i) % P_E for j in range(8)], dtype=torch.int32, device=dev)
+            for i in range(4)]
     rec("dequant_experts_3bit_8x4096x1536_bf16",
-        graph_time_us(torch, lambda: tq.dequant_experts(qp, dids, out_dtype=torch.bfloat16), flush),
+        b2b_graph_us(torch, [lambda q=q: tq.dequant_experts(qp, q, out_dtype=torch.bfloat16) for q in qids]),
         8 * per_exp + 8 * P_H * P_I * 2, shape="8 experts x 4096 x 1536, 3-bit group 64 -> bf16 (codes + scales "
                                                "read, weights written)")
     del qp
@@ -353,13 +441,13 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
     kk = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
     vv = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
     kv_bytes = Hkv * ctx * ((kvc.kw + kvc.vw) * 4 + 2 * (D // KG) * 2)
-    rec("kv_quantize_131072", graph_time_us(torch, lambda: tq.kv_quantize(kvc, kk, vv, pos=0), flush, iters=8),
+    rec("kv_quantize_131072", b2b_graph_us(torch, [lambda: tq.kv_quantize(kvc, kk, vv, pos=0)] * 4),
         2 * ctx * Hkv * D * 2 + kv_bytes, shape="131072 tokens x 8 kv heads x 128, K 8-bit / V 3-bit, group 32")
     del kk, vv
     kvc.length = ctx
     q = torch.randn((32, D), generator=gen, device=dev).to(torch.bfloat16)
     ws = torch.empty(max(int(tq.load().tq_kv_attend_workspace_bytes(32, D, ctx)), 1), dtype=torch.uint8, device=dev)
-    rec("kv_attend_131072", graph_time_us(torch, lambda: tq.kv_attend(kvc, q, ws=ws), flush), kv_bytes,
+    rec("kv_attend_131072", b2b_graph_us(torch, [lambda: tq.kv_attend(kvc, q, ws=ws)] * 8), kv_bytes,
         shape="32 query heads (GQA 4:1) over 131072 cached tokens")
     return out
 
@@ -375,11 +463,16 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill gather-GEMM measurement")
     ap.add_argument("--skip-extras", action="store_true", help="skip the other calls' measurements")
     ap.add_argument("--_oracle-sample", dest="oracle_sample", type=float, default=None)
+    ap.add_argument("--_oracle-procs", dest="oracle_procs", type=int, default=1)
     args = ap.parse_args()
 
     if args.oracle_sample is not None:
-        b, s, desc = oracle_sample(args.oracle_sample)
-        print(json.dumps({"bytes": b, "seconds": s, "desc": desc}))
+        if args.oracle_procs > 1:
+            rate, s = oracle_sample_parallel(args.oracle_sample, args.oracle_procs)
+            print(json.dumps({"bytes": rate * s, "seconds": s}))
+        else:
+            b, s, desc = oracle_sample(args.oracle_sample)
+            print(json.dumps({"bytes": b, "seconds": s, "desc": desc}))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -391,7 +484,8 @@ def main():
                           "2048, ternary group 16 (gate||up gather_qmv + SwiGLU/rotate + down multi_gather_qmv)",
               "experts": E, "top_k": TOPK, "hidden": HIDDEN, "intermediate": INTER, "group": GROUP,
               "tokens_per_step": 1, "bytes_per_step": step_bytes,
-              "cache": "L2 flushed (256 MiB write) before every timed step; 5.5 GB expert bank, fresh routing per step"}
+              "cache": "no flush: inputs larger than L2 (each timed step routes its own token over a 5.5 GB expert "
+                       "bank; the K steps run back to back in one CUDA graph)"}
     metric = "MoE gather_qmv decode packed-weight GB/s (% HBM peak); gather_qmm TFLOP/s"
 
     if args.impl == "reference":
@@ -444,106 +538,107 @@ def main():
 
     aux = torch.cuda.Stream(device=dev)
 
-    def step():  # six calls, one per hot-path step; routing and the input rotation run side by side
+    def step_on(logits, x):  # one call per hot-path step; routing and the input rotation run side by side
         cur = torch.cuda.current_stream()
         aux.wait_stream(cur)
         with torch.cuda.stream(aux):
-            xr = tq.rotate(x_buf, rotH)
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)  # decode reads experts by id
+            xr = tq.rotate(x, rotH)
+        ids, probs, _, _, _ = tq.moe_route(logits, TOPK, sort=False)  # decode reads experts by id
         cur.wait_stream(aux)
         gu = tq.gather_qmv(qgu, xr, ids)
         hr = tq.swiglu_rotate(gu, INTER, rotI)
         yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    def step_serial():  # the same six calls in one stream (measured, not the headline)
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
-        xr = tq.rotate(x_buf, rotH)
+    def step():
+        return step_on(logits_buf, x_buf)
+
+    def step_serial_on(logits, x):  # the same calls in one stream (also the e2e path)
+        ids, probs, _, _, _ = tq.moe_route(logits, TOPK, sort=False)
+        xr = tq.rotate(x, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
         hr = tq.swiglu_rotate(gu, INTER, rotI)
         yd = tq.multi_gather_qmv(qdn, hr, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    def step_fused_down():  # SwiGLU + rotation inside the down matvec (measured, not the headline)
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
-        xr = tq.rotate(x_buf, rotH)
+    def step_serial():
+        return step_serial_on(logits_buf, x_buf)
+
+    def step_fused_down_on(logits, x):  # SwiGLU + rotation inside the down matvec (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits, TOPK, sort=False)
+        xr = tq.rotate(x, rotH)
         gu = tq.gather_qmv(qgu, xr, ids)
         yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    def step_all_fused():  # the input rotation inside gate||up too (measured, not the headline)
-        ids, probs, _, _, _ = tq.moe_route(logits_buf, TOPK, sort=False)
-        gu = tq.gather_qmv_rotate(qgu, x_buf, rotH, ids)
+    def step_all_fused_on(logits, x):  # the input rotation inside gate||up too (measured, not the headline)
+        ids, probs, _, _, _ = tq.moe_route(logits, TOPK, sort=False)
+        gu = tq.gather_qmv_rotate(qgu, x, rotH, ids)
         yd = tq.multi_gather_qmv_swiglu(qdn, gu.view(TOPK, 2 * INTER), rotI, ids.view(-1))
         return tq.moe_combine(yd, probs, TOPK)
 
-    launches_per_step = 6  # route top-k; rotate; gate||up gather; SwiGLU + rotate; down multi-gather; combine
+    # kernels per step: route top-k; rotate; gate||up table-lookup gather + its column-slice sum;
+    # SwiGLU + rotate; down gather (one column slice); combine
+    launches_per_step = 7
 
-    # warm up eagerly (first calls set kernel attributes), then capture the step
-    logits_buf.copy_(logits_all[0:1])
-    x_buf.copy_(x_all[0:1])
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            out_static = step()
-    torch.cuda.current_stream().wait_stream(s)
+    # warm up eagerly (first calls set kernel attributes), then capture the warm-up and the timed steps
+    for i in range(2):
+        step_on(logits_all[i:i + 1], x_all[i:i + 1])
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
+    def capture(lo, hi):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(lo, hi):
+                    step_on(logits_all[i:i + 1], x_all[i:i + 1])
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    g_warm = capture(0, args.warmup)
+    g_timed = capture(args.warmup, nsteps)
+    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    g_warm.replay()
     barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
-        for i in range(nsteps):
-            flush.fill_(i & 0xFF)
-            logits_buf.copy_(logits_all[i:i + 1])
-            x_buf.copy_(x_all[i:i + 1])
-            ev[i][0].record()
-            g.replay()
-            ev[i][1].record()
+        e0.record()
+        g_timed.replay()
+        e1.record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        # keep the GPU busy on the same graph a little longer so the clock sampler sees the load
+        # (outside the events; not part of the timed steps)
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 0.6:
+            g_timed.replay()
+        torch.cuda.synchronize()
     barrier()
-    times = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, nsteps)]
-    t_ms = max_over_ranks(torch, sum(times), world, dev)
+    t_ms = max_over_ranks(torch, e0.elapsed_time(e1), world, dev)
     value = job_gbs(world, args.steps, step_bytes, t_ms)
     clocks = clk.summary()
 
-    # dominant kernel alone: gate||up gather_qmv, one launch per replay, L2 flushed between
-    ids_fixed = torch.tensor([[(3 + 47 * j) % nexp for j in range(TOPK)]], dtype=torch.int32, device=dev)
+    # dominant kernel alone: the gate||up gather on 32 fresh routings, back to back in one graph
+    klog = torch.from_numpy(wl.router_logits(rank_seed(rank) + 11, 32, nexp)).to(dev)
+    kids = [tq.moe_route(klog[i:i + 1], TOPK, sort=False)[0] for i in range(32)]
     xr_fixed = tq.rotate(x_all[0:1], rotH)
-    gs = torch.cuda.Stream(device=dev)
-    gs.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(gs):
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(kg, stream=gs):
-            tq.gather_qmv(qgu, xr_fixed, ids_fixed)
-    torch.cuda.current_stream().wait_stream(gs)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
-    for i in range(40):
-        flush.fill_(i & 0xFF)
-        kev[i][0].record()
-        kg.replay()
-        kev[i][1].record()
-    torch.cuda.synchronize()
-    kt = sorted(kev[i][0].elapsed_time(kev[i][1]) for i in range(5, 40))
-    k_ms = sum(kt) / len(kt)
+    k_us = b2b_graph_us(torch, [lambda i=i: tq.gather_qmv(qgu, xr_fixed, kids[i]) for i in range(32)])
     k_bytes = TOPK * gu_b
-    achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    roofline = {"kernel": "qmv_trit_tc_kernel (gate||up gather_qmv, 8 ternary experts)", "bound": "hbm",
-                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "peak_source": peaks["source"] + " (burst copy)", "traffic": None,
-                "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_ms * 1e3}
+    achieved = k_bytes / (k_us * 1e-6) / 1e9
+    roofline = {"kernel": "qmv_lut_kernel + lut_slice_sum_kernel (gate||up gather_qmv, 8 ternary experts)",
+                "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " (burst copy)",
+                "traffic": None, "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_us,
+                "timing": "32 calls on 32 fresh routings back to back in one CUDA graph, CUDA events around it"}
     tr = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr):
         # DRAM bytes per launch from an ncu capture, valid only while the kernel source is unchanged
@@ -579,19 +674,27 @@ def main():
            "ms_per_step": e2e_ms / args.steps}
 
     prefill = None if args.skip_prefill else measure_prefill(torch, tq, wl, dev, flush, peaks)
-    # the same step with other splits into calls (same inputs; one graph replay each, L2 flushed)
+    # the same step with other splits into calls
     step_variants = None
     if not args.skip_extras:
-        step_variants = {"headline_6_launches_us": graph_time_us(torch, step, flush),
-                         "one_stream_6_launches_us": graph_time_us(torch, step_serial, flush),
-                         "swiglu_in_down_5_launches_us": graph_time_us(torch, step_fused_down, flush),
-                         "rotation_in_gate_up_too_4_launches_us": graph_time_us(torch, step_all_fused, flush)}
+        nv = min(16, nsteps)
+
+        def variant(fn):
+            return b2b_graph_us(torch, [lambda i=i: fn(logits_all[i:i + 1], x_all[i:i + 1]) for i in range(nv)])
+
+        step_variants = {"headline_two_streams_us": variant(step_on),
+                         "one_stream_us": variant(step_serial_on),
+                         "swiglu_in_down_us": variant(step_fused_down_on),
+                         "rotation_in_gate_up_too_us": variant(step_all_fused_on),
+                         "step_isolated_us": graph_time_us(torch, step, flush),
+                         "timing": "back-to-back steps on fresh routings in one CUDA graph (per step); "
+                                   "step_isolated_us: one step replayed alone after a 256 MiB L2 flush"}
     extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
 
     if rank == 0:
         line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+                "vs_baseline": None, "dtype": DTYPE, "data": "synthetic", "config": config,
                 "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "gather_qmm_tflops": prefill["value"] if prefill else None, "prefill": prefill,
