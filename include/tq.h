@@ -370,6 +370,75 @@ tq_status tq_kv_attend_noalloc(const void* q, tq_dtype qdt, int32_t Hq, int32_t 
                                void* stream);
 size_t tq_kv_attend_noalloc_max_scratch_bytes(void);
 
+/* ------------------------------------------------------------------ persisted packed layers (host) */
+
+/* Per-layer tiers and a persisted packed format.
+ * "How it works", "The ternary tier (1.58 bits)": the format marks itself (2^b
+ * codebook entries = bit-packed, 3 = trit-packed), so a model mixes tiers layer
+ * by layer (ternary experts, 4-bit down projections, 3-bit protected layers);
+ * "Configuration that converter and loader share": bit widths are chosen per
+ * layer from its name, the loader recomputes the same choice, and a layer's
+ * width is recovered from the size of its saved codebook, never from a config
+ * field.  The weight-reservoir page: a flat, page-aligned file of each layer's
+ * packed indices and scales with a small header (shape, rotation seed), loaded
+ * byte-identical to what was written.  All of this is host code: buffers are
+ * host memory, and nothing touches the GPU. */
+
+#define TQ_LAYER_NAME_BYTES 64
+
+/* A quantized layer as stored: name (NUL-terminated), a bank of `experts`
+ * matrices [rows, cols] with `group`-wide fp16 scales, codes at row_stride_words
+ * words per row, the rotation (dim = cols, Hadamard block, sign seed) and the
+ * codebook: `levels` fp64 centroids, ascending.  codes: host uint32
+ * [experts][rows][row_stride_words]; scales: host fp16 bits
+ * [experts][rows][cols/group]. */
+typedef struct tq_layer_desc_t {
+    char name[TQ_LAYER_NAME_BYTES];
+    int32_t experts, rows, cols, group;
+    int64_t row_stride_words;
+    int32_t levels;
+    int32_t rot_dim, rot_block;
+    uint64_t rot_seed;
+    const double* centroids;
+    const uint32_t* codes;
+    const uint16_t* scales;
+} tq_layer_desc_t;
+
+/* Tier (codebook size and group) of each layer class.  A layer belongs to the
+ * first class whose marker its name contains: "down_proj", "expert", "mlp",
+ * "attn"; any other layer (e.g. a protected embedding or head) is "other". */
+typedef struct tq_tier_policy_t {
+    int32_t down_levels, down_group;
+    int32_t expert_levels, expert_group;
+    int32_t mlp_levels, mlp_group;
+    int32_t attn_levels, attn_group;
+    int32_t other_levels, other_group;
+} tq_tier_policy_t;
+
+/* The tier of layer `name` under `policy`: *levels and *group.  TQ_ERR_INVALID
+ * for NULL arguments or a policy entry that is not a supported book / group. */
+tq_status tq_layer_tier(const char* name, const tq_tier_policy_t* policy, int32_t* levels, int32_t* group);
+
+/* Writes n_layers layers to `path` (overwritten): a 64-byte header, one 256-byte
+ * record per layer, then each layer's codebook, codes and scales, each blob
+ * starting on a 4096-byte boundary with zero bytes between.  Writing the same
+ * layers again gives the same bytes.  TQ_ERR_INVALID for an inconsistent layer
+ * (levels not 3/4/8/16/256, rot_dim != cols, block not dividing cols, stride too
+ * short, unterminated name, NULL data) or an I/O error. */
+tq_status tq_pack_file_write(const char* path, const tq_layer_desc_t* layers, int32_t n_layers);
+
+/* Reads the layer table of `path`: *n_layers, and the first min(cap, n) layers'
+ * metadata into infos (pointers left NULL).  Each layer's levels is the number of
+ * centroids stored in its codebook blob.  TQ_ERR_INVALID for a file that is not a
+ * packed-layer file of this version or whose table points past its end. */
+tq_status tq_pack_file_info(const char* path, int32_t* n_layers, tq_layer_desc_t* infos, int32_t cap);
+
+/* Reads layer `index` of `path` into host buffers sized from tq_pack_file_info:
+ * centroids double[levels], codes uint32[experts*rows*row_stride_words], scales
+ * uint16[experts*rows*(cols/group)]. */
+tq_status tq_pack_file_read_layer(const char* path, int32_t index, double* centroids, uint32_t* codes,
+                                  uint16_t* scales);
+
 /* Waits for `stream`, reads the device error word and clears it.
  * Returns TQ_OK if it was 0, TQ_ERR_TIMEOUT if TQ_DEVERR_TIMEOUT is set, else
  * TQ_ERR_DEVICE; *bits (host, may be NULL) receives the word. */

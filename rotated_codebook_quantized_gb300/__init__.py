@@ -41,6 +41,17 @@ class tq_qweight_t(ctypes.Structure):
                 ("expert_stride_scales", _i64), ("cb", tq_codebook_t)]
 
 
+class tq_layer_desc_t(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 64), ("experts", _i32), ("rows", _i32), ("cols", _i32), ("group", _i32),
+                ("row_stride_words", _i64), ("levels", _i32), ("rot_dim", _i32), ("rot_block", _i32),
+                ("rot_seed", ctypes.c_uint64), ("centroids", _c_p), ("codes", _c_p), ("scales", _c_p)]
+
+
+class tq_tier_policy_t(ctypes.Structure):
+    _fields_ = [(n, _i32) for n in ("down_levels", "down_group", "expert_levels", "expert_group", "mlp_levels",
+                                    "mlp_group", "attn_levels", "attn_group", "other_levels", "other_group")]
+
+
 _P = ctypes.POINTER
 # name -> (restype, argtypes), exactly the declarations of include/tq.h
 _SIGS = {
@@ -81,6 +92,10 @@ _SIGS = {
                                     _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "tq_kv_attend_noalloc_max_scratch_bytes": (_sz, []),
     "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
+    "tq_layer_tier": (_i32, [ctypes.c_char_p, _P(tq_tier_policy_t), _P(_i32), _P(_i32)]),
+    "tq_pack_file_write": (_i32, [ctypes.c_char_p, _P(tq_layer_desc_t), _i32]),
+    "tq_pack_file_info": (_i32, [ctypes.c_char_p, _P(_i32), _P(tq_layer_desc_t), _i32]),
+    "tq_pack_file_read_layer": (_i32, [ctypes.c_char_p, _i32, _c_p, _c_p, _c_p]),
     "tq_selftest_trit_decode": (_i32, [_u32, _u32, _c_p, _c_p]),
 }
 
@@ -498,3 +513,82 @@ def selftest_trit_decode(first: int = 0, count: int = 3 ** 20) -> int:
     m = torch.zeros(1, dtype=torch.int64, device="cuda")
     _check(load().tq_selftest_trit_decode(first, count, _ptr(m), _stream()), "tq_selftest_trit_decode")
     return int(m.item())
+
+
+# ---------------------------------------------------------------- per-layer tiers and the packed file
+
+# "How it works": ternary experts, 4-bit down projections, 3-bit protected layers; group 16 for
+# MLP and expert layers.
+DEFAULT_TIERS = {"down": (16, 16), "expert": (3, 16), "mlp": (8, 16), "attn": (8, 64), "other": (8, 64)}
+
+
+def tier_policy(tiers: dict | None = None) -> tq_tier_policy_t:
+    t = dict(DEFAULT_TIERS, **(tiers or {}))
+    return tq_tier_policy_t(t["down"][0], t["down"][1], t["expert"][0], t["expert"][1], t["mlp"][0], t["mlp"][1],
+                            t["attn"][0], t["attn"][1], t["other"][0], t["other"][1])
+
+
+def layer_tier(name: str, policy: tq_tier_policy_t | None = None) -> tuple[int, int]:
+    """(codebook size, group) of layer `name` under the tier policy."""
+    lv, g = _i32(0), _i32(0)
+    pol = policy if policy is not None else tier_policy()
+    _check(load().tq_layer_tier(name.encode(), ctypes.byref(pol), ctypes.byref(lv), ctypes.byref(g)), "tq_layer_tier")
+    return int(lv.value), int(g.value)
+
+
+class PackedLayer:
+    """A layer as stored in a packed file: host numpy arrays and their metadata."""
+
+    def __init__(self, name, codes, scales, centroids, group, rot_block, rot_seed):
+        self.name = name
+        self.codes = np.ascontiguousarray(codes, dtype=np.uint32)        # [experts, rows, row_stride]
+        self.scales = np.ascontiguousarray(scales).view(np.uint16)        # [experts, rows, cols/group]
+        self.centroids = np.ascontiguousarray(centroids, dtype=np.float64)
+        self.experts, self.rows, self.row_stride = self.codes.shape
+        self.group = int(group)
+        self.cols = self.scales.shape[-1] * self.group
+        self.rot_block, self.rot_seed = int(rot_block), int(rot_seed)
+
+    @property
+    def levels(self) -> int:
+        return len(self.centroids)
+
+    def qweight(self, device="cuda") -> "QWeight":
+        """The layer on the device (its codebook's thresholds are the midpoints of the centroids)."""
+        torch = _torch()
+        c = self.centroids
+        cb = Codebook(self.levels, device=device, centroids=c, thresholds=(c[1:] + c[:-1]) / 2)
+        codes = torch.from_numpy(self.codes.view(np.int32)).to(device)
+        scales = torch.from_numpy(self.scales.view(np.int16)).to(device)
+        return QWeight(codes, scales, self.experts, self.rows, self.cols, self.group, cb, row_stride=self.row_stride)
+
+
+def save_packed(path: str, layers: list[PackedLayer]) -> None:
+    descs = (tq_layer_desc_t * max(len(layers), 1))()
+    for d, L in zip(descs, layers):
+        d.name = L.name.encode()
+        d.experts, d.rows, d.cols, d.group = L.experts, L.rows, L.cols, L.group
+        d.row_stride_words, d.levels = L.row_stride, L.levels
+        d.rot_dim, d.rot_block, d.rot_seed = L.cols, L.rot_block, L.rot_seed
+        d.centroids = L.centroids.ctypes.data
+        d.codes = L.codes.ctypes.data
+        d.scales = L.scales.ctypes.data
+    _check(load().tq_pack_file_write(path.encode(), descs, len(layers)), "tq_pack_file_write")
+
+
+def load_packed(path: str) -> list[PackedLayer]:
+    lib = load()
+    n = _i32(0)
+    _check(lib.tq_pack_file_info(path.encode(), ctypes.byref(n), None, 0), "tq_pack_file_info")
+    infos = (tq_layer_desc_t * max(n.value, 1))()
+    _check(lib.tq_pack_file_info(path.encode(), ctypes.byref(n), infos, n.value), "tq_pack_file_info")
+    out = []
+    for i in range(n.value):
+        d = infos[i]
+        c = np.zeros(d.levels, np.float64)
+        codes = np.zeros((d.experts, d.rows, d.row_stride_words), np.uint32)
+        scales = np.zeros((d.experts, d.rows, d.cols // d.group), np.uint16)
+        _check(lib.tq_pack_file_read_layer(path.encode(), i, c.ctypes.data, codes.ctypes.data, scales.ctypes.data),
+               "tq_pack_file_read_layer")
+        out.append(PackedLayer(d.name.decode(), codes, scales, c, d.group, d.rot_block, d.rot_seed))
+    return out
