@@ -23,6 +23,10 @@ where a float decides an integer: the nearest-centroid decision is taken in
 fp32 (the precision the GPU kernels compute in), so both sides decide in the
 same precision.
 
+The dense QR-fallback rotation (``rotation_dense``) draws its Gaussian matrix
+from SplitMix64 through the Box-Muller transform; the CUDA library implements
+the same generator from its published definition on its own side.
+
 Parity pins: every public function here is pinned by a ``-m "not gpu"`` test
 against something other than itself (published tables, closed forms,
 invariants, brute force).  No function is unpinned.
@@ -203,6 +207,64 @@ def rotation_block(dim: int) -> int:
     1536 -> 512, 4096 -> 4096).  This is exactly orthonormal for every dim.
     """
     return dim & (-dim)
+
+
+def rotation_kind(dim: int) -> str:
+    """Which rotation a layer of input dimension ``dim`` takes (a reading of the pages).
+
+    The weight-reservoir page falls back from the fast Hadamard transform to a
+    QR-derived dense rotation for dimensions the transform cannot take.  With
+    the block-diagonal reading above every dim has a Hadamard rotation, but a
+    block below 64 mixes too few values to make a group Gaussian; such dims
+    (e.g. 400 = 16 x 25, odd dims) take the dense rotation.
+    """
+    return "hadamard" if rotation_block(dim) >= 64 else "dense"
+
+
+def splitmix64_array(seed: int, n: int) -> np.ndarray:
+    """The first ``n`` SplitMix64 outputs as a uint64 array (the stream of
+    ``splitmix64_stream``, computed for all indices at once: state_i = seed + (i+1) gamma)."""
+    with np.errstate(over="ignore"):
+        i = np.arange(1, n + 1, dtype=np.uint64)
+        z = np.uint64(seed & _MASK64) + i * np.uint64(0x9E3779B97F4A7C15)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def gaussian_stream(seed: int, n: int) -> np.ndarray:
+    """``n`` standard normal draws from the SplitMix64 stream of ``seed`` by the Box-Muller transform
+    (Box & Muller 1958).
+
+    The pages derive a dense rotation from a seed (weight-reservoir page, the QR
+    fallback) without naming the generator; the reading taken: draws 2p and 2p+1
+    come from outputs 2p and 2p+1, u = (output >> 11) / 2^53 in [0, 1), and
+    r = sqrt(-2 ln(1 - u_2p)), z_2p = r cos(2 pi u_2p+1), z_2p+1 = r sin(2 pi u_2p+1).
+    """
+    m = n + (n & 1)
+    x = splitmix64_array(seed, m)
+    u = (x >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log1p(-u1))
+    z = np.empty(m)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return z[:n]
+
+
+def rotation_dense(seed: int, dim: int) -> np.ndarray:
+    """Dense Haar-random rotation R [dim, dim] for the QR fallback.
+
+    Weight-reservoir page: a rotation for a dimension the fast transform cannot
+    take is derived from the seed by a QR decomposition (numpy.linalg.qr of a
+    random matrix).  Reading: G[i, j] = gaussian_stream(seed)[i * dim + j], G = Q U
+    with the diagonal of U made positive (the unique factorisation, which makes Q
+    Haar-distributed), R = Q; x_rot = R x and W_rot = W R^T as for Hadamard layers.
+    """
+    G = gaussian_stream(seed, dim * dim).reshape(dim, dim)
+    Q, U = np.linalg.qr(G)  # library primitive (LAPACK Householder)
+    return Q * np.sign(np.diag(U))[None, :]
 
 
 def rotation_matrix(signs: np.ndarray, block: int) -> np.ndarray:
