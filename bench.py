@@ -383,6 +383,8 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
     Algorithmic bytes: unpadded code words + fp16 scales of the matrices a call reads (each distinct
     expert once), KV codes + scales for attention, inputs read + codes and scales written for the
     encoders, weights written for dequant_experts."""
+    import numpy as np
+
     hbm = peaks["hbm_gbs"]
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000)
@@ -434,6 +436,20 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
         8 * per_exp + 8 * P_H * P_I * 2, shape="8 experts x 4096 x 1536, 3-bit group 64 -> bf16 (codes + scales "
                                                "read, weights written)")
     del qp
+    # dense (QR-fallback) rotation of a 2000-wide layer (2000 = 16 x 125: Hadamard blocks of 16 only):
+    # one decode input per call over 16 rotations in turn (256 MB > L2), and the encode's fp64-sum rotation
+    # of 2048 weight rows
+    Dd = 2000
+    rots = [tq.DenseRotation(Dd, R=np.linalg.qr(np.random.default_rng(i).normal(size=(Dd, Dd)))[0], device=dev)
+            for i in range(16)]
+    xd = torch.randn((1, Dd), generator=gen, device=dev)
+    rec("rotate_dense_2000_T1", b2b_graph_us(torch, [lambda r=r: tq.rotate_dense(xd, r) for r in rots]),
+        Dd * Dd * 4 + 2 * Dd * 4, shape="R [2000, 2000] f32 times one input (fp32 sums)")
+    Wd = torch.randn((2048, Dd), generator=gen, device=dev) * 0.02
+    us = b2b_graph_us(torch, [lambda: tq.rotate_dense(Wd, rots[0], precise=True)] * 2)
+    out["rotate_dense_2000_encode_2048_rows"] = dict(us=us, gflops=2.0 * 2048 * Dd * Dd / (us * 1e3),
+                                                     shape="2048 rows x R^T, fp64 sums (the encode's rotation)")
+    del rots, Wd
     # KV cache: compress 131072 tokens x 8 heads x 128 (8-bit K, 3-bit V, group 32), then one decode read
     ctx, Hkv, D, KG = 131072, 8, 128, 32
     kvc = tq.KVCache(ctx, Hkv, D, KG, tq.Codebook(256, device=dev), tq.Codebook(8, device=dev),

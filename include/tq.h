@@ -139,6 +139,18 @@ tq_status tq_codebook(int32_t levels, double* centroids, double* thresholds);
  * signs: host int8[dim]. */
 tq_status tq_rotation_signs(uint64_t seed, int32_t dim, int8_t* signs);
 
+/* Dense rotation for a dimension the block Hadamard transform mixes too little.
+ * Weight-reservoir page: such a layer's rotation is derived from its seed by a
+ * QR decomposition of a random matrix (the QR fallback).  G[i][j] is the
+ * (i*dim + j)-th standard normal draw of the seed's SplitMix64 stream through
+ * the Box-Muller transform (draws 2p, 2p+1 from outputs 2p, 2p+1, u = (output
+ * >> 11) / 2^53, r = sqrt(-2 ln(1 - u_2p)), cos / sin of 2 pi u_2p+1); G = QU
+ * with U's diagonal positive, computed in fp64 by Householder reflections on the
+ * host's threads; R = Q, written row-major to host double[dim * dim].  The layer
+ * then stores W R^T and multiplies R x.  Cost: about 3 dim^3 flops on the host
+ * (seconds at dim 2000).  dim: 1 .. 16384. */
+tq_status tq_rotation_dense(uint64_t seed, int32_t dim, double* R);
+
 /* ------------------------------------------------------------------ device entry points */
 
 /* x_rot = R x for `rows` vectors.
@@ -148,6 +160,16 @@ tq_status tq_rotation_signs(uint64_t seed, int32_t dim, int8_t* signs);
  * [rows, rot->dim] of dtype ydt (f32, bf16 or f16), may not alias x. */
 tq_status tq_rotate(const tq_rotation_t* rot, const void* x, tq_dtype xdt, int64_t rows,
                     void* x_rot, tq_dtype ydt, void* stream);
+
+/* y[r] = R x[r] for `rows` vectors with a dense rotation (the QR fallback above).
+ * R: device f32 [dim, dim] row-major.  x: device [rows, dim] of xdt (f32, bf16 or
+ * f16).  y: device f32 [rows, dim], may not alias x.  precise != 0 accumulates in
+ * fp64 (for encoding: the rotated value then carries only its final fp32
+ * rounding); 0 accumulates in fp32 (a decode input).  To encode such a layer,
+ * rotate its rows with precise = 1 and pass them to tq_quantize with the
+ * identity rotation (block 1, all signs +1). */
+tq_status tq_rotate_dense(const float* R, int32_t dim, const void* x, tq_dtype xdt, int64_t rows, float* y,
+                          int32_t precise, void* stream);
 
 /* Fused encode of weight rows: rotate, per-group RMS, snap, pack.
  * "How it works", "Quantizing a weight, with no data" (all four steps).

@@ -92,6 +92,8 @@ _SIGS = {
                                     _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "tq_kv_attend_noalloc_max_scratch_bytes": (_sz, []),
     "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
+    "tq_rotation_dense": (_i32, [ctypes.c_uint64, _i32, _P(ctypes.c_double)]),
+    "tq_rotate_dense": (_i32, [_c_p, _i32, _c_p, _i32, _i64, _c_p, _i32, _c_p]),
     "tq_layer_tier": (_i32, [ctypes.c_char_p, _P(tq_tier_policy_t), _P(_i32), _P(_i32)]),
     "tq_pack_file_write": (_i32, [ctypes.c_char_p, _P(tq_layer_desc_t), _i32]),
     "tq_pack_file_info": (_i32, [ctypes.c_char_p, _P(_i32), _P(tq_layer_desc_t), _i32]),
@@ -191,6 +193,14 @@ def rotation_signs(seed: int, dim: int) -> np.ndarray:
     return s
 
 
+def rotation_dense(seed: int, dim: int) -> np.ndarray:
+    """Host fp64 dense rotation [dim, dim] of the QR fallback (see include/tq.h, tq_rotation_dense)."""
+    R = np.zeros((dim, dim), dtype=np.float64)
+    _check(load().tq_rotation_dense(ctypes.c_uint64(seed), dim, R.ctypes.data_as(_P(ctypes.c_double))),
+           "tq_rotation_dense")
+    return R
+
+
 # ---------------------------------------------------------------- device descriptors
 
 class Codebook:
@@ -224,6 +234,21 @@ class Rotation:
         return tq_rotation_t(self.dim, self.block, self.signs.data_ptr())
 
 
+class DenseRotation:
+    """The QR-fallback rotation of a dimension on the device (fp32 [dim, dim]), from its seed or given."""
+
+    def __init__(self, dim: int, seed: int | None = None, R=None, device="cuda"):
+        torch = _torch()
+        if R is None:
+            R = rotation_dense(seed, dim)
+        self.dim = int(dim)
+        self.R = torch.tensor(np.asarray(R, np.float32), device=device)
+
+    def identity(self, device="cuda") -> "Rotation":
+        """The identity rotation of this dim (block 1, signs +1): what tq_quantize takes after rotate_dense."""
+        return Rotation(self.dim, 1, signs=np.ones(self.dim, np.int8), device=device)
+
+
 class QWeight:
     """A bank of quantized matrices [experts, rows, cols] as written by ``quantize``."""
 
@@ -250,6 +275,21 @@ def rotate(x, rot: Rotation, out_dtype=None):
     _check(load().tq_rotate(ctypes.byref(r), _ptr(x), _dt(x), x.numel() // rot.dim, _ptr(out), _dt(out), _stream()),
            "tq_rotate")
     return out
+
+
+def rotate_dense(x, rot: DenseRotation, precise: bool = False):
+    """R x for every row of x (f32 out); precise accumulates in fp64."""
+    torch = _torch()
+    _contig(x, "x")
+    out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _check(load().tq_rotate_dense(_ptr(rot.R), rot.dim, _ptr(x), _dt(x), x.numel() // rot.dim, _ptr(out),
+                                  int(precise), _stream()), "tq_rotate_dense")
+    return out
+
+
+def quantize_dense(W, group: int, rot: DenseRotation, cb: Codebook, row_stride: int | None = None):
+    """Encode rows of W with the dense rotation: rotate (fp64 sums), then group RMS, snap and pack."""
+    return quantize(rotate_dense(W, rot, precise=True), group, rot.identity(device=W.device), cb, row_stride)
 
 
 def quantize(W, group: int, rot: Rotation, cb: Codebook, row_stride: int | None = None):

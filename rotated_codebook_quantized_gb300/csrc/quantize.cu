@@ -403,6 +403,46 @@ __global__ void __launch_bounds__(256, 4) kv_quantize8_kernel(const void* __rest
 // (group / E <= 32) so the group's sum of squares is a warp-shuffle reduction.
 // Values per thread: the most (up to 16) that still give whole warps, so that more of the
 // transform runs in registers and shuffles and fewer stages go through shared memory.
+// Encode of rows whose rotation is diagonal (block 1: the signs alone), for widths the fused
+// kernel's layout does not take (e.g. rows already rotated by a dense rotation): one CTA per row,
+// a thread per group for the RMS and the codes, then a thread per word for the packing.
+__global__ void __launch_bounds__(256) quantize_diag_kernel(const void* __restrict__ W, int wdt, int cols, int group,
+                                                            const int8_t* __restrict__ signs,
+                                                            const float* __restrict__ thresholds, int levels,
+                                                            uint32_t* __restrict__ codes,
+                                                            uint16_t* __restrict__ scales, int64_t row_stride) {
+    extern __shared__ float smem[];
+    float* thr = smem;                                       // levels-1 thresholds
+    uint8_t* cd = reinterpret_cast<uint8_t*>(smem + 256);   // [cols] codes of the row
+    const int nthr = levels - 1;
+    for (int i = threadIdx.x; i < nthr; i += blockDim.x) thr[i] = thresholds[i];
+    __syncthreads();
+    const int64_t row = blockIdx.x;
+    const int64_t off = row * cols;
+    const int ngroups = cols / group;
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        float ss = 0.f;
+        for (int i = 0; i < group; ++i) {
+            const int k = g * group + i;
+            const float v = load_as_float(W, off + k, wdt) * (float)signs[k];
+            ss += v * v;
+        }
+        const float s = sqrtf(ss * (1.0f / (float)group));
+        scales[row * ngroups + g] = __half_as_ushort(__float2half_rn(s));
+        for (int i = 0; i < group; ++i) {
+            const int k = g * group + i;
+            const float v = load_as_float(W, off + k, wdt) * (float)signs[k];
+            const float u = s > 0.f ? __fdiv_rn(v, s) : 0.f;
+            cd[k] = (uint8_t)snap_code(u, thr, nthr);
+        }
+    }
+    __syncthreads();
+    const int cw = levels == 3 ? 20 : (levels == 8 ? 10 : 32 / (31 - __clz(levels)));
+    const int bits = 31 - __clz(levels);
+    for (int64_t j = threadIdx.x; j < row_stride; j += blockDim.x)
+        codes[row * row_stride + j] = pack_word(cd, cols, (int)j, levels, cw, bits);
+}
+
 int pick_e(int dim, int block, int group) {
     for (int e = 16; e >= 1; e >>= 1)
         if (e <= block && dim % (32 * e) == 0 && dim / e <= 1024 && group <= 32 * e) return e;
@@ -427,6 +467,13 @@ extern "C" tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int3
     if (rows == 0) return TQ_OK;
     if (!W || !codes || !scales) return TQ_ERR_INVALID;
     const int e = pick_e(cols, rot->block, group);
+    if ((e == 0 || cols > 16384) && rot->block == 1 && cols <= 65536) {  // a diagonal rotation
+        const size_t smem_d = 256 * 4 + (size_t)cols;
+        if (ensure_smem((const void*)quantize_diag_kernel, smem_d) != cudaSuccess) return TQ_ERR_CUDA;
+        quantize_diag_kernel<<<(unsigned)rows, 256, smem_d, as_stream(stream)>>>(
+            W, wdt, cols, group, rot->signs, cb->thresholds, cb->levels, codes, scales, row_stride_words);
+        return launch_status();
+    }
     if (e == 0 || cols > 16384) return TQ_ERR_UNSUPPORTED;
     const int threads = cols / e;
     const size_t smem = fwht_pad_floats(cols) * 4 + 256 * 4 + (size_t)cols;

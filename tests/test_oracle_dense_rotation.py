@@ -67,3 +67,14 @@ def test_planted_mistake_in_qr_sign_convention_is_caught():
     if np.all(np.diag(Q.T @ G) > 0):
         pytest.skip("LAPACK happened to return the positive-diagonal factorisation")
     assert not np.all(np.diag(Q.T @ G) > 0)
+
+
+@pytest.mark.parametrize("dim,seed", [(5, 3), (50, 11), (208, 7), (400, 1234)])
+def test_library_dense_rotation_matches_oracle(dim, seed):
+    """The library's host Householder QR of its own Gaussian stream against the oracle's numpy QR."""
+    tq = pytest.importorskip("rotated_codebook_quantized_gb300")
+    try:
+        tq.load()
+    except RuntimeError:
+        pytest.skip("libtq.so not built")
+    np.testing.assert_allclose(tq.rotation_dense(seed, dim), o.rotation_dense(seed, dim), rtol=0, atol=1e-12)
