@@ -468,6 +468,50 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
     return out
 
 
+def measure_streaming(torch, tq, wl, dev, qgu, steps=32):
+    """Expert streaming: 64 gate||up experts (ternary 4096 x 7168, group 16) in pinned host
+    memory, 16 device slots, one top-8 token per step: map the routing (LRU, one pair of
+    host-to-device copies per missing expert), then gather_qmv from the slots.  Two routings:
+    'cold', where every step misses all 8 experts (the copy rate over the CPU-GPU link), and
+    Zipf(1.1)-skewed router logits (the hit rate an LRU reaches on a skewed router).  Timed with
+    CUDA events around all steps on the current stream; the host plans each step while the
+    previous one's copies and gather run."""
+    import numpy as np
+
+    NE, SLOTS = 64, 16
+    hc = qgu.codes[:NE].cpu().pin_memory()
+    hs = qgu.scales[:NE].cpu().pin_memory()
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    x = torch.randn((1, HIDDEN), generator=g, device=dev)
+    lg = wl.router_logits(SEED + 77, steps + 4, NE, zipf=1.1)
+    routings = {"cold": [np.arange(8 * i, 8 * i + 8) % NE for i in range(steps + 4)],
+                "zipf_1.1": [np.argsort(-lg[i])[:TOPK] for i in range(steps + 4)]}
+    out = {}
+    for name, ids_list in routings.items():
+        cache = tq.ExpertCache(hc, hs, NE, qgu.rows, qgu.cols, qgu.group, qgu.cb, SLOTS, row_stride=qgu.row_stride,
+                               device=dev)
+        for i in range(4):  # warm-up steps
+            cache.gather_qmv(x, torch.from_numpy(ids_list[i].astype(np.int32)).view(1, -1).to(dev))
+        torch.cuda.synchronize()
+        h0, m0, b0 = cache.stats()
+        ids_dev = [torch.from_numpy(ids_list[i].astype(np.int32)).view(1, -1) for i in range(4, steps + 4)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            cache.gather_qmv(x, ids_dev[i])
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        h1, m1, b1 = cache.stats()
+        out[name] = {"ms_per_step": ms / steps, "misses_per_step": (m1 - m0) / steps,
+                     "hit_rate": (h1 - h0) / max(1, (h1 - h0) + (m1 - m0)),
+                     "h2d_gbs": (b1 - b0) / (ms * 1e-3) / 1e9, "h2d_bytes_per_step": (b1 - b0) / steps}
+        del cache
+    out["config"] = "64 experts x [4096, 7168] ternary group 16 in pinned host memory, 16 device slots, top-8, T=1"
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -706,6 +750,7 @@ def main():
                          "timing": "back-to-back steps on fresh routings in one CUDA graph (per step); "
                                    "step_isolated_us: one step replayed alone after a 256 MiB L2 flush"}
     extras = None if args.skip_extras else measure_extras(torch, tq, wl, dev, flush, peaks, qdn)
+    streaming = None if args.skip_extras else measure_streaming(torch, tq, wl, dev, qgu)
 
     if rank == 0:
         line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -714,7 +759,7 @@ def main():
                 "frac_of_hbm_peak": value / peaks["hbm_gbs"], "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "gather_qmm_tflops": prefill["value"] if prefill else None, "prefill": prefill,
-                "extras": extras, "step_variants": step_variants, "wall_s_timed_loop": wall}
+                "extras": extras, "expert_stream": streaming, "step_variants": step_variants, "wall_s_timed_loop": wall}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

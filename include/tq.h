@@ -461,10 +461,73 @@ tq_status tq_pack_file_info(const char* path, int32_t* n_layers, tq_layer_desc_t
 tq_status tq_pack_file_read_layer(const char* path, int32_t index, double* centroids, uint32_t* codes,
                                   uint16_t* scales);
 
+/* ------------------------------------------------------------------ expert streaming (host bank, device LRU) */
+
+/* Expert streaming from host memory.
+ * "How it works", "Expert streaming": a Mixture-of-Experts bank larger than the
+ * device budget stays outside it, and only the experts a step routes to are
+ * brought in, through a least-recently-used cache, with results bit-identical
+ * to running the whole bank resident.  "Running a 1T-Parameter Model on a
+ * Laptop": expert loading reads only the routed experts.
+ *
+ * Here the bank is a tq_qweight_t whose codes and scales are HOST memory
+ * (pinned, so that copies run asynchronously over the CPU-GPU link), experts
+ * back to back (expert_stride_words = rows*row_stride_words, expert_stride_scales
+ * = rows*cols/group).  The cache owns no memory on either side: dev_codes
+ * (uint32 [slots][rows][row_stride_words]) and dev_scales (fp16 bits
+ * [slots][rows][cols/group]) are caller-allocated device buffers that must stay
+ * valid for the cache's lifetime.  A device-side view of the slots is the bank
+ * with codes/scales replaced by dev_codes/dev_scales and experts = slots; the
+ * gather entry points run on it with ids remapped to slots. */
+typedef struct tq_expert_cache tq_expert_cache;
+
+/* Creates a cache of `slots` device slots over `host_bank` (copied; the
+ * arrays it points to are not).  TQ_ERR_INVALID for NULL arguments, slots <= 0
+ * or a malformed bank; TQ_ERR_UNSUPPORTED for experts not stored back to back. */
+tq_status tq_expert_cache_create(const tq_qweight_t* host_bank, int32_t slots, uint32_t* dev_codes,
+                                 uint16_t* dev_scales, tq_expert_cache** out);
+
+/* Frees the bookkeeping (not the buffers).  NULL is a no-op. */
+void tq_expert_cache_destroy(tq_expert_cache* cache);
+
+/* One step of LRU bookkeeping, host only: for ids[0..n) (host int32 expert ids,
+ * repeats allowed) writes slots[i] (host int32), the slot holding expert ids[i]
+ * after the step, and miss[i] (host uint8) = 1 where ids[i] is the first
+ * occurrence of an expert that was not cached and must be copied into slots[i].
+ * Experts used in the step are never evicted by the step; the victim of a miss is
+ * the lowest empty slot if any, else the slot used least recently (the lowest
+ * of equals).  TQ_ERR_INVALID for
+ * an id outside [0, experts) (nothing changes) or more distinct uncached experts
+ * than slots not used by the step (no slot changes content). */
+tq_status tq_expert_cache_plan(tq_expert_cache* cache, const int32_t* ids, int32_t n, int32_t* slots, uint8_t* miss);
+
+/* tq_expert_cache_plan, then for every miss two cudaMemcpyAsync host-to-device
+ * copies on `stream` (the expert's code words, then its scales) into its slot.
+ * Work on `stream` after the call sees the experts in place.  TQ_ERR_CUDA if a
+ * copy cannot be enqueued. */
+tq_status tq_expert_cache_map(tq_expert_cache* cache, const int32_t* ids, int32_t n, int32_t* slots, void* stream);
+
+/* Counters since creation: distinct-per-step hits and misses, and bytes copied
+ * (any pointer may be NULL). */
+tq_status tq_expert_cache_stats(const tq_expert_cache* cache, int64_t* hits, int64_t* misses,
+                                int64_t* bytes_copied);
+
 /* Waits for `stream`, reads the device error word and clears it.
  * Returns TQ_OK if it was 0, TQ_ERR_TIMEOUT if TQ_DEVERR_TIMEOUT is set, else
  * TQ_ERR_DEVICE; *bits (host, may be NULL) receives the word. */
 tq_status tq_check_error(uint32_t* err, uint32_t* bits, void* stream);
+
+/* Test hook for the bounded waits of the tensor-core kernels (tq_gather_qmm,
+ * tq_qmv_tc): every wait of a pipeline role on another (an mbarrier phase)
+ * gives up after `cycles` SM clock cycles, raises TQ_DEVERR_TIMEOUT in the
+ * call's error word (tq_check_error then returns TQ_ERR_TIMEOUT) and the CTA
+ * stops: each role drains the copies and MMAs it has in flight (bounded by the
+ * default budget, whatever `cycles` is), TMEM is freed and the kernel returns,
+ * leaving the output incomplete.  Applies to launches after the call, process
+ * wide.  cycles < 0 restores the default, 2^31 cycles (about a second); 0 makes
+ * every wait whose phase has not already completed give up at once.  Not for
+ * production use: a short budget aborts work that would have finished. */
+tq_status tq_set_wait_budget(int64_t cycles);
 
 /* Exhaustive self-check of the divide-free base-3 digit decoder used by the
  * ternary kernels: decodes every word in [first, first+count) (count words,

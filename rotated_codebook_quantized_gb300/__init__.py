@@ -92,12 +92,18 @@ _SIGS = {
                                     _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "tq_kv_attend_noalloc_max_scratch_bytes": (_sz, []),
     "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
+    "tq_set_wait_budget": (_i32, [_i64]),
     "tq_rotation_dense": (_i32, [ctypes.c_uint64, _i32, _P(ctypes.c_double)]),
     "tq_rotate_dense": (_i32, [_c_p, _i32, _c_p, _i32, _i64, _c_p, _i32, _c_p]),
     "tq_layer_tier": (_i32, [ctypes.c_char_p, _P(tq_tier_policy_t), _P(_i32), _P(_i32)]),
     "tq_pack_file_write": (_i32, [ctypes.c_char_p, _P(tq_layer_desc_t), _i32]),
     "tq_pack_file_info": (_i32, [ctypes.c_char_p, _P(_i32), _P(tq_layer_desc_t), _i32]),
     "tq_pack_file_read_layer": (_i32, [ctypes.c_char_p, _i32, _c_p, _c_p, _c_p]),
+    "tq_expert_cache_create": (_i32, [_P(tq_qweight_t), _i32, _c_p, _c_p, _P(_c_p)]),
+    "tq_expert_cache_destroy": (None, [_c_p]),
+    "tq_expert_cache_plan": (_i32, [_c_p, _c_p, _i32, _c_p, _c_p]),
+    "tq_expert_cache_map": (_i32, [_c_p, _c_p, _i32, _c_p, _c_p]),
+    "tq_expert_cache_stats": (_i32, [_c_p, _P(_i64), _P(_i64), _P(_i64)]),
     "tq_selftest_trit_decode": (_i32, [_u32, _u32, _c_p, _c_p]),
 }
 
@@ -548,6 +554,11 @@ def check_error(err) -> int:
     return int(bits.value)
 
 
+def set_wait_budget(cycles: int) -> None:
+    """Test hook: cycle budget of the tensor-core kernels' bounded waits (-1: the default)."""
+    _check(load().tq_set_wait_budget(int(cycles)), "tq_set_wait_budget")
+
+
 def selftest_trit_decode(first: int = 0, count: int = 3 ** 20) -> int:
     torch = _torch()
     m = torch.zeros(1, dtype=torch.int64, device="cuda")
@@ -632,3 +643,82 @@ def load_packed(path: str) -> list[PackedLayer]:
                "tq_pack_file_read_layer")
         out.append(PackedLayer(d.name.decode(), codes, scales, c, d.group, d.rot_block, d.rot_seed))
     return out
+
+
+# ---------------------------------------------------------------- expert streaming
+
+class ExpertCache:
+    """Experts of a bank held in host memory, streamed into ``slots`` device slots (LRU).
+
+    ``codes`` (int32/uint32 [experts, rows, row_stride]) and ``scales`` (16-bit
+    [experts, rows, cols/group]) are host arrays: pinned torch CPU tensors for
+    ``map`` (the copies are asynchronous), or numpy arrays for ``plan`` alone.
+    ``view`` is the slot bank on the device, a QWeight with ``slots`` experts
+    that the gather entry points run on with ids remapped to slots.
+    """
+
+    def __init__(self, codes, scales, experts: int, rows: int, cols: int, group: int, cb: Codebook, slots: int,
+                 row_stride: int | None = None, device="cuda"):
+        self.host_codes, self.host_scales = codes, scales
+        self.row_stride = int(row_stride if row_stride is not None else row_stride_words(cb.levels, cols))
+        self.experts, self.rows, self.cols, self.group, self.slots = experts, rows, cols, group, int(slots)
+        self.cb = cb
+        cp = codes.data_ptr() if hasattr(codes, "data_ptr") else codes.ctypes.data
+        sp = scales.data_ptr() if hasattr(scales, "data_ptr") else scales.ctypes.data
+        host = tq_qweight_t(cp, sp, experts, rows, cols, group, self.row_stride, rows * self.row_stride,
+                            rows * (cols // group), cb.c())
+        self.view = None
+        dc = ds = None
+        if device is not None:
+            torch = _torch()
+            dcodes = torch.empty((self.slots, rows, self.row_stride), dtype=torch.int32, device=device)
+            dscales = torch.empty((self.slots, rows, cols // group), dtype=torch.int16, device=device)
+            self.view = QWeight(dcodes, dscales, self.slots, rows, cols, group, cb, row_stride=self.row_stride)
+            dc, ds = dcodes.data_ptr(), dscales.data_ptr()
+        h = _c_p()
+        _check(load().tq_expert_cache_create(ctypes.byref(host), self.slots, dc, ds, ctypes.byref(h)),
+               "tq_expert_cache_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.tq_expert_cache_destroy(h)
+            self._h = None
+
+    @staticmethod
+    def _ids(ids) -> np.ndarray:
+        if hasattr(ids, "detach"):
+            ids = ids.detach().to("cpu").numpy()
+        return np.ascontiguousarray(np.asarray(ids).reshape(-1), dtype=np.int32)
+
+    def plan(self, ids):
+        """LRU bookkeeping only (host): (slot of each id, 1 where the id is a first miss)."""
+        a = self._ids(ids)
+        slots = np.zeros(a.size, np.int32)
+        miss = np.zeros(a.size, np.uint8)
+        _check(load().tq_expert_cache_plan(self._h, a.ctypes.data, a.size, slots.ctypes.data, miss.ctypes.data),
+               "tq_expert_cache_plan")
+        return slots, miss
+
+    def map(self, ids):
+        """Brings the experts of ``ids`` into the slots on the current stream; their slots (host int32)."""
+        a = self._ids(ids)
+        slots = np.zeros(a.size, np.int32)
+        _check(load().tq_expert_cache_map(self._h, a.ctypes.data, a.size, slots.ctypes.data, _stream()),
+               "tq_expert_cache_map")
+        return slots
+
+    def stats(self) -> tuple[int, int, int]:
+        """(hits, misses, bytes copied) since creation."""
+        h, m, b = _i64(0), _i64(0), _i64(0)
+        _check(load().tq_expert_cache_stats(self._h, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)),
+               "tq_expert_cache_stats")
+        return int(h.value), int(m.value), int(b.value)
+
+    def gather_qmv(self, x_rot, ids, out_dtype=None, err=None):
+        """gather_qmv of the host bank: maps ``ids`` [T, k], then gathers from the slots."""
+        torch = _torch()
+        shape = tuple(ids.shape)
+        slots = torch.from_numpy(self.map(ids)).reshape(shape).pin_memory().to(x_rot.device, non_blocking=True)
+        return gather_qmv(self.view, x_rot, slots, out_dtype=out_dtype, err=err)

@@ -36,6 +36,9 @@ inline tq_status launch_status() {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Cycle budget of each bounded wait in the tensor-core kernels launched now (tq_set_wait_budget).
+long long wait_budget();
+
 // Raise a kernel's dynamic shared-memory limit once per process (not on every
 // launch, so launches can be captured into CUDA graphs without extra API calls).
 inline cudaError_t ensure_smem(const void* kernel, size_t bytes) {

@@ -14,9 +14,10 @@
 // diagonal (the unique factorisation, which makes Q Haar-distributed).  R = Q.
 //
 // Device: y[r, i] = sum_j R[i, j] x[r, j], a register-tiled GEMM on the CUDA
-// cores (64 x 64 outputs per CTA, 4 x 4 per thread), accumulating in fp64 for
-// encodes (the code decision must not move by more than the rounding of the
-// rotated value) or in fp32 for a decode input.
+// cores (64 x 64 outputs per CTA, 4 x 4 per thread), or for up to 8 rows a
+// matvec that streams R once (one warp per output dimension), accumulating in
+// fp64 for encodes (the code decision must not move by more than the rounding
+// of the rotated value) or in fp32 for a decode input.
 #include <math.h>
 #include <stdint.h>
 
@@ -180,6 +181,58 @@ __global__ void __launch_bounds__(256) rotate_dense_kernel(const float* __restri
     }
 }
 
+// Few rows (a decode input): one warp per output dimension i streams row i of R once with
+// 16-byte loads (dim % 4 == 0) and dots it with every input row held in shared memory.
+constexpr int kGvRows = 8, kGvWarps = 8;
+
+template <class ACC>
+__global__ void __launch_bounds__(256) rotate_dense_gemv_kernel(const float* __restrict__ R, int dim,
+                                                                const void* __restrict__ x, int xdt, int rows,
+                                                                float* __restrict__ y) {
+    extern __shared__ __align__(16) float xs[];  // [rows][dim]
+    for (int e = threadIdx.x; e < rows * dim; e += blockDim.x) xs[e] = load_as_float(x, e, xdt);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kGvWarps + (threadIdx.x >> 5);
+    if (i >= dim) return;
+    const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)i * dim);
+    const int n4 = dim / 4;
+    ACC acc[kGvRows];
+#pragma unroll
+    for (int r = 0; r < kGvRows; ++r) acc[r] = 0;
+    constexpr int U = 8;  // loads in flight per lane
+    for (int b = 0; b < n4; b += 32 * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = b + u * 32 + lane;
+            v[u] = q < n4 ? __ldg(r4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = b + u * 32 + lane;
+            if (q >= n4) break;
+#pragma unroll
+            for (int r = 0; r < kGvRows; ++r) {
+                if (r >= rows) break;
+                const float4 xv = reinterpret_cast<const float4*>(xs + (size_t)r * dim)[q];
+                acc[r] = fma((ACC)v[u].x, (ACC)xv.x, acc[r]);
+                acc[r] = fma((ACC)v[u].y, (ACC)xv.y, acc[r]);
+                acc[r] = fma((ACC)v[u].z, (ACC)xv.z, acc[r]);
+                acc[r] = fma((ACC)v[u].w, (ACC)xv.w, acc[r]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kGvRows; ++r) {
+        if (r >= rows) break;
+        ACC a = acc[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) y[(size_t)r * dim + i] = (float)a;
+    }
+}
+
 }  // namespace
 
 extern "C" tq_status tq_rotate_dense(const float* R, int32_t dim, const void* x, tq_dtype xdt, int64_t rows, float* y,
@@ -187,10 +240,19 @@ extern "C" tq_status tq_rotate_dense(const float* R, int32_t dim, const void* x,
     if (!R || dim <= 0 || rows < 0 || (xdt != TQ_F32 && xdt != TQ_BF16 && xdt != TQ_F16)) return TQ_ERR_INVALID;
     if (rows == 0) return TQ_OK;
     if (!x || !y || (const void*)y == x) return TQ_ERR_INVALID;
+    cudaStream_t st = as_stream(stream);
+    const size_t xs_bytes = (size_t)rows * dim * 4;
+    if (rows <= kGvRows && dim % 4 == 0 && aligned(R, 16) && xs_bytes <= 48 * 1024) {
+        const unsigned g = (unsigned)((dim + kGvWarps - 1) / kGvWarps);
+        if (precise)
+            rotate_dense_gemv_kernel<double><<<g, 32 * kGvWarps, xs_bytes, st>>>(R, dim, x, xdt, (int)rows, y);
+        else
+            rotate_dense_gemv_kernel<float><<<g, 32 * kGvWarps, xs_bytes, st>>>(R, dim, x, xdt, (int)rows, y);
+        return launch_status();
+    }
     const int64_t gy = (rows + kTN - 1) / kTN;
     if (gy > 65535) return TQ_ERR_UNSUPPORTED;
     const dim3 grid((dim + kTM - 1) / kTM, (unsigned)gy);
-    cudaStream_t st = as_stream(stream);
     if (precise)
         rotate_dense_kernel<double><<<grid, 256, 0, st>>>(R, dim, x, xdt, rows, y);
     else

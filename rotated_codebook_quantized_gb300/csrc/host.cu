@@ -1,5 +1,6 @@
 // Host-side entry points: status names, format sizes, the Gaussian Lloyd-Max
 // codebook, the seeded rotation signs and the device error word.
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -156,6 +157,22 @@ extern "C" tq_status tq_rotation_signs(uint64_t seed, int32_t dim, int8_t* signs
         z ^= z >> 31;
         signs[i] = (z >> 63) ? (int8_t)-1 : (int8_t)1;
     }
+    return TQ_OK;
+}
+
+// ---------------------------------------------------------------- bounded-wait budget
+
+namespace {
+constexpr long long kDefaultWaitCycles = 1ll << 31;  // about a second at GB300 clocks
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+}  // namespace
+
+namespace tq {
+long long wait_budget() { return g_wait_cycles.load(std::memory_order_relaxed); }
+}  // namespace tq
+
+extern "C" tq_status tq_set_wait_budget(int64_t cycles) {
+    g_wait_cycles.store(cycles < 0 ? kDefaultWaitCycles : (long long)cycles, std::memory_order_relaxed);
     return TQ_OK;
 }
 

@@ -155,6 +155,7 @@ struct QmmParams {
     int ydt;
     uint32_t* err;
     const float* colscale;  // split-K form: per input row, the factor applied to its outputs
+    long long wait_cycles;  // budget of each bounded wait (wait_budget() at launch)
 };
 
 template <int LEVELS, int G, int XT>
@@ -262,11 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
                 item_coords(item, e, mt, nt, i0, nvalid);
                 const int ninst = (nvalid + 15) & ~15;
                 const uint32_t idesc = f16_idesc(XT, ninst);
-                if (!mbar_wait(tile_empty, (tile_it & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(tile_empty, (tile_it & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 tc_fence_after();
                 for (int kc = 0; kc < nk; ++kc, ++it) {
                     const int s = it % kStages;
-                    if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(a0 + s * kABytes), bd = sw128_desc(b0 + s * kBBytes);
 #pragma unroll
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
             int prev_s = -1;
             for (int kc = 0; kc < nk; ++kc, ++it) {
                 const int s = it % kStages;
-                if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 const uint32_t dst0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
         // All decoder threads meet here; bounded, so an aborting thread cannot strand the others.
         auto dec_sync = [&]() -> bool {
             mbar_arrive(decbar);
-            const bool r = mbar_wait(decbar, dec_phase, abort_flag);
+            const bool r = mbar_wait(decbar, dec_phase, abort_flag, p.wait_cycles);
             dec_phase ^= 1;
             return r;
         };
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
                     if (kc < nk && ok) {
                         if (kc + PF - 1 < nk) load(kc + PF - 1, wb[(u + PF - 1) % PF], sb[(u + PF - 1) % PF]);
                         const int s = it % kStages;
-                        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) {
+                        if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag, p.wait_cycles)) {
                             ok = false;
                         } else {
                             uint32_t out[16];
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(const QmmParams
             }
             if (!ok) break;
             // epilogue: TMEM -> registers -> y (rows of the sorted pairs)
-            if (!mbar_wait(tile_full, tile_it & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(tile_full, tile_it & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
             tc_fence_after();
             if (!dec_sync()) { ok = false; break; }  // rowscale visible
             const int m = quarter * 32 + lane;
@@ -769,13 +770,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const int ncols = ksplit ? ninst : (me == 0 ? min(ninst, 128) : ninst - 128);
                 const uint32_t idesc = f16_idesc(XT, ncols > 0 ? ncols : 16);
                 const int buf = tile_it & 1;
-                if (!mbar_wait(tile_empty + buf, ((tile_it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(tile_empty + buf, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * kBuf + me * kHalf);
                 const uint32_t boff = ksplit ? 0u : (uint32_t)(me * 128 * 128);  // B rows of thread 1's columns
                 for (int kc = kb; kc < ke; ++kc, ++it) {
                     const int s = it % kStages;
-                    if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag)) {
+                    if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag, p.wait_cycles)) {
                         ok = false;
                         break;
                     }
@@ -813,7 +814,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 for (int kc = I.kb; kc < I.ke; ++kc, ++it) {
                     if ((int)(it % kBWarps) != bw) continue;
                     const int s = it % kStages;
-                    if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(empty + s, ((it / kStages) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                     uint64_t* fb = full + s;
                     mbar_expect_tx(fb, (uint32_t)box_rows * 128u);
                     tma_load_2d(b0 + s * kBBytes, &tm.b[bi], kc * kBK, i0, fb);
@@ -837,7 +838,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const int e = I.e, mt = I.mt;
                 for (int c = I.c0; c < I.c1; ++c, ++cc) {
                     const int slot = cc % kChunkSlots;
-                    if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                     mbar_expect_tx(cfull + slot, (uint32_t)kChunkCodeBytes);
                     tma_load_3d(c0 + slot * kChunkBytes, &tm.c, c * 32, mt * kBM, e, cfull + slot);
                 }
@@ -860,7 +861,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             bool ok = true;
             for (int c = I.c0; c < I.c1; ++c, ++cc) {
                 const int slot = cc % kChunkSlots;
-                if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(cempty + slot, ((cc / kChunkSlots) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 const int wlo = (c * CPC / G) >> 1;
                 const int ghi = min(ngroups - 1, ((c + 1) * CPC - 1) / G);
                 const int nw = (ghi >> 1) - wlo + 1;  // 1..SW words per row
@@ -902,14 +903,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int c = I.c0; c < I.c1 && ok; ++c, ++cc) {
                 const int k0 = c * SPC, nsub = min(SPC, I.ke - k0);
                 const int slot = cc % kChunkSlots;
-                if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(cfull + slot, (cc / kChunkSlots) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 const uint32_t crow = crow0 + slot * kChunkBytes, srow = srow0 + slot * kChunkBytes;
                 const int gbase = (c * CPC / G) & ~1;  // group at word 0 of the chunk's scale rows
                 for (int sub = (int)((it ^ (uint32_t)grp) & 1u); sub < nsub; sub += 2) {
                     const uint32_t sit = it + (uint32_t)sub;
                     const int kc = k0 + sub;
                     const int s = sit % kStages;
-                    if (!pre && !mbar_wait(empty + s, ((sit / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    if (!pre && !mbar_wait(empty + s, ((sit / kStages) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                     {
                         const uint32_t nit = sit + 2;  // this group's next stage
                         pre = mbar_peek(empty + nit % kStages, ((nit / kStages) & 1) ^ 1);
@@ -983,7 +984,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         for (bool have = first_item(I); have; have = next_item(I), ++tile_it) {
             const int mt = I.mt, i0 = I.i0, nvalid = I.nvalid;
             const int buf = tile_it & 1;
-            if (!mbar_wait(tile_full + buf, (tile_it >> 1) & 1, abort_flag)) break;
+            if (!mbar_wait(tile_full + buf, (tile_it >> 1) & 1, abort_flag, p.wait_cycles)) break;
             tc_fence_after();
             const int64_t ybase = (int64_t)i0 * p.rows + mt * kBM + m;
             const bool ksplit = ((nvalid + 15) & ~15) <= 128 && I.ke - I.kb >= 2;  // as the MMA threads decided
@@ -1285,6 +1286,7 @@ extern "C" tq_status tq_gather_qmm(const tq_qweight_t* w, const void* x, tq_dtyp
     if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return TQ_ERR_INVALID;
     if (P == 0) return TQ_OK;
     QmmParams p{};
+    p.wait_cycles = wait_budget();
     p.codes = w->codes;
     p.scales = w->scales;
     p.row_stride = w->row_stride_words;
@@ -1348,6 +1350,7 @@ extern "C" tq_status tq_qmv_tc(const tq_qweight_t* w, const float* x_rot, int32_
     const size_t need = tq_qmv_tc_workspace_bytes(T, w->cols);
     if (!ws || ws_bytes < need || !aligned(ws, 16)) return TQ_ERR_INVALID;
     QmmParams p{};
+    p.wait_cycles = wait_budget();
     p.codes = w->codes;
     p.scales = w->scales;
     p.row_stride = w->row_stride_words;

@@ -66,14 +66,15 @@ TQ_DEVFN bool mbar_peek(uint64_t* b, uint32_t parity) {
 }
 
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
-// (and raises the CTA's abort flag) if it did not within kWaitCycles or if
-// another role already aborted.
-TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+// (and raises the CTA's abort flag) if it did not within `budget` cycles
+// (kWaitCycles unless the launch carries another budget) or if another role
+// already aborted.
+TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, long long budget = kWaitCycles) {
     if (mbar_test(b, parity)) return true;  // common case first: no clock read, no suspension
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }

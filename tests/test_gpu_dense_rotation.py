@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.mark.parametrize("dim,rows,precise", [(400, 33, True), (400, 3, False), (1040, 70, True), (50, 5, False)])
+@pytest.mark.parametrize("dim,rows,precise", [(400, 33, True), (400, 3, False), (1040, 70, True), (50, 5, False),
+                                             (2000, 1, False), (2000, 6, True), (1040, 9, False), (1996, 2, True)])
 def test_rotate_dense(lib, dim, rows, precise):
     seed = 40 + dim
     x = wl.rng(seed, rows).normal(size=(rows, dim)).astype(np.float32)
