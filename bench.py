@@ -427,7 +427,12 @@ def measure_extras(torch, tq, wl, dev, flush, peaks, qdn):
     distinct = sum(int(torch.unique(p).numel()) for p in pids) / len(pids)
     rec("multi_gather_3bit_T8", b2b_graph_us(torch, [lambda p=p: tq.multi_gather_qmv(qp, hp, p) for p in pids] * 2),
         distinct * per_exp, shape="64 pairs (8 tokens x top-8 of 128) x 4096 x 1536, 3-bit group 64",
-        distinct_experts=distinct, bytes_counted="distinct experts x bytes per expert (each read once)")
+        distinct_experts=distinct, bytes_counted="distinct experts x bytes per expert (each read once)",
+        path="pairs grouped by expert (each expert decoded once for up to 4 of its pairs)")
+    rec("multi_gather_3bit_T8_per_pair",
+        b2b_graph_us(torch, [lambda p=p: tq.multi_gather_qmv(qp, hp, p, use_ws=False) for p in pids] * 2),
+        distinct * per_exp, shape="the same call without scratch: one item per pair (repeats re-read)",
+        distinct_experts=distinct, bytes_counted="distinct experts x bytes per expert")
     # dense rotated-domain weights of 8 experts of the same bank, for a regular matmul (bf16 out)
     qids = [torch.tensor([(7 + 13 * j + 8 * i) % P_E for j in range(8)], dtype=torch.int32, device=dev)
             for i in range(4)]
@@ -512,6 +517,81 @@ def measure_streaming(torch, tq, wl, dev, qgu, steps=32):
     return out
 
 
+CASES = ("gate_up", "down", "dense_t1", "multi_t8", "dequant", "quantize", "kv_quantize", "kv_attend")
+
+
+def run_case(name: str):
+    """A few launches of one call at the workloads' shapes, on a small bank, for profiler captures
+    (ncu -k <kernel> -s <skip> -c <count>): every input is resident before the first launch of the
+    call, and each launch reads inputs larger than L2.  Prints one line and exits."""
+    import torch
+
+    import rotated_codebook_quantized_gb300 as tq
+    from rotated_codebook_quantized_gb300 import workloads as wl
+
+    tq.load()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7000)
+    out = None
+    if name in ("gate_up", "down"):
+        qgu, qdn = make_bank(torch, tq, dev, 32)  # 32 experts: 8 per call, 4 disjoint routings
+        if name == "gate_up":
+            x = torch.randn((1, HIDDEN), generator=gen, device=dev)
+            for i in range(3):
+                ids = torch.tensor([[(8 * i + j) % 32 for j in range(TOPK)]], dtype=torch.int32, device=dev)
+                out = tq.gather_qmv(qgu, x, ids)
+        else:
+            h = torch.randn((TOPK, INTER), generator=gen, device=dev)
+            for i in range(3):
+                ids = torch.tensor([(8 * i + j) % 32 for j in range(TOPK)], dtype=torch.int32, device=dev)
+                out = tq.multi_gather_qmv(qdn, h, ids)
+    elif name == "dense_t1":  # 8 copies of the 11008 x 4096 3-bit matrix (150 MB), T = 1
+        qs = [random_bit_bank(torch, tq, dev, gen, 1, 11008, 4096, 8, 128) for _ in range(8)]
+        x = torch.randn((1, 4096), generator=gen, device=dev)
+        for _ in range(2):
+            for q in qs:
+                out = tq.qmv(q, x)
+    elif name in ("multi_t8", "dequant"):  # the prefill down bank: 128 x [4096, 1536], 3-bit group 64
+        qp = random_bit_bank(torch, tq, dev, gen, P_E, P_H, P_I, 8, P_G)
+        if name == "multi_t8":
+            plog = torch.from_numpy(wl.router_logits(P_SEED, 32, P_E, zipf=1.1)).to(dev)
+            hp = torch.randn((8 * P_K, P_I), generator=gen, device=dev)
+            for i in range(4):
+                ids = tq.moe_route(plog[8 * i:8 * i + 8], P_K, sort=False)[0].view(-1)
+                out = tq.multi_gather_qmv(qp, hp, ids)
+        else:
+            for i in range(3):
+                ids = torch.tensor([(7 + 13 * j + 8 * i) % P_E for j in range(8)], dtype=torch.int32, device=dev)
+                out = tq.dequant_experts(qp, ids, out_dtype=torch.bfloat16)
+    elif name == "quantize":  # two 11008 x 4096 bf16 inputs in turn (180 MB)
+        Ws = [(torch.randn((11008, 4096), generator=gen, device=dev) * 0.02).to(torch.bfloat16) for _ in range(2)]
+        rot = tq.Rotation(4096, 4096, seed=11, device=dev)
+        cb = tq.Codebook(8, device=dev)
+        for i in range(3):
+            out = tq.quantize(Ws[i % 2], 128, rot, cb)[0]
+    elif name in ("kv_quantize", "kv_attend"):  # 131072 tokens x 8 kv heads x 128, K 8-bit / V 3-bit
+        ctx, Hkv, D, KG = 131072, 8, 128, 32
+        kvc = tq.KVCache(ctx, Hkv, D, KG, tq.Codebook(256, device=dev), tq.Codebook(8, device=dev),
+                         tq.Rotation(D, D, seed=13, device=dev), device=dev)
+        kk = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+        vv = torch.randn((ctx, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+        for _ in range(3 if name == "kv_quantize" else 1):
+            tq.kv_quantize(kvc, kk, vv, pos=0)
+        kvc.length = ctx
+        if name == "kv_attend":
+            del kk, vv
+            q = torch.randn((32, D), generator=gen, device=dev).to(torch.bfloat16)
+            for _ in range(3):
+                out = tq.kv_attend(kvc, q)
+        else:
+            out = kvc.kcodes
+    else:
+        raise SystemExit(f"unknown case {name}; one of {', '.join(CASES)}")
+    torch.cuda.synchronize()
+    print(json.dumps({"case": name, "ok": True, "checksum": float(out.float().abs().sum())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,9 +602,15 @@ def main():
     ap.add_argument("--experts", type=int, default=E, help="decode bank size (smaller only for profiling captures)")
     ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill gather-GEMM measurement")
     ap.add_argument("--skip-extras", action="store_true", help="skip the other calls' measurements")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run a few launches of one call for a profiler capture, then exit")
     ap.add_argument("--_oracle-sample", dest="oracle_sample", type=float, default=None)
     ap.add_argument("--_oracle-procs", dest="oracle_procs", type=int, default=1)
     args = ap.parse_args()
+
+    if args.case is not None:
+        run_case(args.case)
+        return
 
     if args.oracle_sample is not None:
         if args.oracle_procs > 1:

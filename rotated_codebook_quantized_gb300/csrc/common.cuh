@@ -39,6 +39,31 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 // Cycle budget of each bounded wait in the tensor-core kernels launched now (tq_set_wait_budget).
 long long wait_budget();
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
+// before it in the stream is still running: it calls pdl_wait() before it reads or writes any
+// memory that kernel may touch (pdl_wait returns once that kernel has completed and its writes
+// are visible; launched without the attribute it returns at once), and pdl_trigger() as soon as
+// its own successor may be scheduled.  Chained this way each launch's setup overlaps the tail of
+// the one before, inside CUDA graphs too.
+TQ_DEVFN void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+TQ_DEVFN void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <class... KArgs, class... Args>
+inline tq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 // Raise a kernel's dynamic shared-memory limit once per process (not on every
 // launch, so launches can be captured into CUDA graphs without extra API calls).
 inline cudaError_t ensure_smem(const void* kernel, size_t bytes) {

@@ -22,6 +22,8 @@ template <int kPer>  // experts per lane: E <= 32 * kPer
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ probs,
                                                          int32_t* __restrict__ counts) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
@@ -123,6 +125,8 @@ __global__ void __launch_bounds__(256) route_compact_kernel(const int32_t* __res
 
 __global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ probs,
                                const int32_t* __restrict__ pair_pos, int k, int H, void* out, int odt) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.y;
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= H) return;
@@ -153,11 +157,17 @@ extern "C" tq_status tq_moe_route(const float* logits, int32_t T, int32_t E, int
     if (T > 0) {
         const int warps = 8;
         const dim3 grid((T + warps - 1) / warps), block(warps * 32);
-        if (E <= 128) route_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
-        else if (E <= 256) route_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
-        else if (E <= 512) route_topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
-        else route_topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
-        tq_status s = launch_status();
+        // without sorting the top-k kernel is the call's only launch: a programmatic dependent of
+        // the previous kernel (with sorting it follows the counts' memset)
+        auto go = [&](auto kern) -> tq_status {
+            if (!sort) return launch_pdl(kern, grid, block, 0, st, logits, T, E, k, ids, probs, counts);
+            kern<<<grid, block, 0, st>>>(logits, T, E, k, ids, probs, counts);
+            return launch_status();
+        };
+        tq_status s = E <= 128 ? go(route_topk_kernel<4>)
+                      : E <= 256 ? go(route_topk_kernel<8>)
+                      : E <= 512 ? go(route_topk_kernel<16>)
+                                 : go(route_topk_kernel<32>);
         if (s != TQ_OK) return s;
     }
     if (!sort) return TQ_OK;
@@ -173,6 +183,6 @@ extern "C" tq_status tq_moe_combine(const float* y, const float* probs, const in
     if (T < 0 || k <= 0 || H <= 0 || !(odt == TQ_F32 || odt == TQ_BF16)) return TQ_ERR_INVALID;
     if (T == 0) return TQ_OK;
     if (!y || !probs || !out || T > 65535) return TQ_ERR_INVALID;
-    combine_kernel<<<dim3((H + 255) / 256, T), 256, 0, as_stream(stream)>>>(y, probs, pair_pos, k, H, out, odt);
-    return launch_status();
+    return launch_pdl(combine_kernel, dim3((H + 255) / 256, T), dim3(256), 0, as_stream(stream), y, probs, pair_pos, k,
+                      H, out, (int)odt);
 }

@@ -4,6 +4,8 @@
 // every routed expert reads the shared input), polar_multi_gather_qmv (a
 // different input per expert), the dense quantized layer, and
 // polar_dequant_experts ("anything else": decode, then a regular matmul).
+#include <algorithm>
+
 #include "qmv_impl.cuh"
 
 using namespace tq;
@@ -129,12 +131,109 @@ size_t items_workspace(const tq_qweight_t* w, int64_t n_items) {
 
 }  // namespace
 
+namespace {
+
+// Multi-gather of bit-packed books, pairs grouped by expert: a record holds an expert and up to
+// kGroupNV of its pairs, and the matvec decodes each record's weights once for all of them.
+constexpr int kGroupNV = 4;
+
+bool groups_apply(const tq_qweight_t* w, int64_t P) {
+    return w && (w->cb.levels == 4 || w->cb.levels == 8 || w->cb.levels == 16) && P >= 2 && w->experts >= 1 &&
+           w->experts <= (1 << 20);
+}
+
+// Workspace of the grouping: records (2 + P * (1 + NV) ints), then per expert its pair count,
+// fill counter and first record (3 * experts ints).
+size_t groups_workspace(const tq_qweight_t* w, int64_t P) {
+    if (!groups_apply(w, P)) return 0;
+    return ((size_t)(2 + P * (1 + kGroupNV)) + 3 * (size_t)w->experts) * 4 + 16;
+}
+
+// One CTA: count the pairs of each expert, lay out each expert's records (experts in ascending
+// order), then place every pair in a slot of its expert's records.  The slot order within an
+// expert follows atomics, which changes nothing in the results (each pair's sums are its own).
+// A pair whose id is outside the bank gets a zero output row and raises BAD_ID.
+__global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                           int32_t* __restrict__ groups, int32_t* __restrict__ cnt,
+                                                           void* y, int rows, int ydt, uint32_t* err) {
+    constexpr int NV = kGroupNV;
+    __shared__ int part[1024];
+    __shared__ int any_bad;
+    int32_t* fill = cnt + E;
+    int32_t* first = fill + E;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid == 0) any_bad = 0;
+    for (int e = tid; e < E; e += nt) cnt[e] = fill[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < P; i += nt) {
+        const int e = __ldg(ids + i);
+        if (e >= 0 && e < E) atomicAdd(cnt + e, 1);
+        else any_bad = 1;
+    }
+    __syncthreads();
+    // records per expert, exclusive prefix over the experts (a contiguous range per thread)
+    const int per = (E + nt - 1) / nt, e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (cnt[e] + NV - 1) / NV;
+    part[tid] = local;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int t = 0; t < nt; ++t) {
+            const int v = part[t];
+            part[t] = acc;
+            acc += v;
+        }
+        groups[0] = acc;
+        groups[1] = 0;
+    }
+    __syncthreads();
+    int run = part[tid];
+    for (int e = e0; e < e1; ++e) {
+        first[e] = run;
+        run += (cnt[e] + NV - 1) / NV;
+    }
+    const int ng = groups[0];
+    for (int i = tid; i < ng * NV; i += nt) groups[2 + (i / NV) * (1 + NV) + 1 + i % NV] = -1;
+    __syncthreads();
+    for (int i = tid; i < P; i += nt) {
+        const int e = __ldg(ids + i);
+        if (e < 0 || e >= E) continue;
+        const int slot = atomicAdd(fill + e, 1);
+        int32_t* rec = groups + 2 + (int64_t)(first[e] + slot / NV) * (1 + NV);
+        rec[0] = e;
+        rec[1 + slot % NV] = i;
+    }
+    if (!any_bad) return;  // uniform
+    if (tid == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
+    for (int i = 0; i < P; ++i) {
+        const int e = __ldg(ids + i);
+        if (e >= 0 && e < E) continue;
+        for (int r = tid; r < rows; r += nt) store_from_float(y, (int64_t)i * rows + r, ydt, 0.f);
+    }
+}
+
+tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaStream_t st) {
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    int32_t* groups = reinterpret_cast<int32_t*>(b);
+    int32_t* cnt = groups + 2 + (size_t)P * (1 + kGroupNV);
+    group_pairs_kernel<<<1, 1024, 0, st>>>(p.ids, P, w->experts, groups, cnt, p.y, p.rows, p.ydt, p.err);
+    tq_status s = launch_status();
+    if (s != TQ_OK) return s;
+    p.mode = kModeGroups;
+    p.groups = groups;
+    // at most P records (one per pair); launches past the actual count return at once
+    return run(p, w->group, kGroupNV, P, st);
+}
+
+}  // namespace
+
 extern "C" size_t tq_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t T, int32_t k) {
     return T > 0 && k > 0 ? items_workspace(w, (int64_t)T * k) : 0;
 }
 
 extern "C" size_t tq_multi_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t P) {
-    return items_workspace(w, P);
+    return std::max(items_workspace(w, P), groups_workspace(w, P));
 }
 
 extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
@@ -166,6 +265,9 @@ extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_r
     p.mode = kModeMulti;
     p.ids = ids;
     p.k = 1;
+    const size_t gneed = groups_workspace(w, P);
+    if (gneed > 0 && ws && ws_bytes >= gneed && aligned(ws, 16))
+        return run_groups(p, w, P, ws, as_stream(stream));
     return run_items(p, w->group, P, ws, ws_bytes, as_stream(stream));
 }
 
@@ -207,49 +309,77 @@ extern "C" tq_status tq_multi_gather_qmv_swiglu(const tq_qweight_t* w, const flo
 
 namespace {
 
-// One CTA per (selected expert, row): each thread decodes whole words.
+// One CTA per (selected expert, run of up to kDqRows rows), in two passes over
+// shared memory: each thread decodes whole words into one code byte per column;
+// then each thread writes 8 consecutive columns (one group, as 8 divides the
+// group) as a single 16-byte store for 16-bit outputs (two for f32), so a warp
+// writes 512 contiguous bytes per instruction.
+constexpr int kDqRows = 4;
+
 __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ codes,
                                                       const uint16_t* __restrict__ scales, int64_t row_stride,
                                                       int64_t esw, int64_t ess, int rows, int cols, int group,
                                                       int experts, const float* __restrict__ centroids, int levels,
-                                                      const int32_t* __restrict__ ids, void* out, int odt,
-                                                      uint32_t* err) {
+                                                      const int32_t* __restrict__ ids, void* out, int odt, int rpc,
+                                                      int cpad, uint32_t* err) {
+    extern __shared__ __align__(16) uint8_t dq[];  // [rpc][cpad] code bytes
     __shared__ float lut[256];
     for (int i = threadIdx.x; i < levels; i += blockDim.x) lut[i] = centroids[i];
-    __syncthreads();
-    const int n = blockIdx.x;
+    const int n0 = blockIdx.x * rpc;
+    const int nr = min(rpc, rows - n0);
     const int64_t i_sel = blockIdx.y;
     const int e = ids[i_sel];
-    const int64_t obase = (i_sel * rows + n) * (int64_t)cols;
     const bool bad = e < 0 || e >= experts;
     if (bad && threadIdx.x == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
     const int cw = levels == 3 ? 20 : (levels == 8 ? 10 : 32 / (31 - __clz(levels)));
     const int bits = 31 - __clz(levels);
     const int nw = (cols + cw - 1) / cw;
-    const uint32_t* wr = codes + (bad ? 0 : (int64_t)e * esw + (int64_t)n * row_stride);
-    const uint16_t* sr = scales + (bad ? 0 : (int64_t)e * ess + (int64_t)n * (cols / group));
-    for (int j = threadIdx.x; j < nw; j += blockDim.x) {
-        const uint32_t w = bad ? 0u : wr[j];
+    const uint32_t* w0 = codes + (bad ? 0 : (int64_t)e * esw + (int64_t)n0 * row_stride);
+    for (int t = threadIdx.x; t < nr * nw; t += blockDim.x) {
+        const int r = t / nw, j = t - r * nw;
+        const uint32_t w = bad ? 0u : __ldg(w0 + (int64_t)r * row_stride + j);
+        uint8_t* d = dq + r * cpad + j * cw;  // cpad >= nw * cw: the tail of the last word lands in padding
         if (levels == 3) {
             const TritHalves th = trit_split(w);
             uint32_t Fh = th.hi, Fl = th.lo;
-            uint32_t d[20];
-            for (int t = 0; t < 10; ++t) d[19 - t] = trit_next_int(Fh);
-            for (int t = 0; t < 10; ++t) d[9 - t] = trit_next_int(Fl);
-            for (int i = 0; i < 20; ++i) {
-                const int kk = j * 20 + i;
-                if (kk < cols)
-                    store_from_float(out, obase + kk, odt,
-                                     bad ? 0.f : half_bits_to_float(sr[kk / group]) * lut[d[i]]);
-            }
+#pragma unroll
+            for (int q = 0; q < 10; ++q) d[19 - q] = (uint8_t)trit_next_int(Fh);
+#pragma unroll
+            for (int q = 0; q < 10; ++q) d[9 - q] = (uint8_t)trit_next_int(Fl);
         } else {
-            for (int i = 0; i < cw; ++i) {
-                const int kk = j * cw + i;
-                if (kk < cols) {
-                    const uint32_t c = (w >> (bits * i)) & ((1u << bits) - 1u);
-                    store_from_float(out, obase + kk, odt, bad ? 0.f : half_bits_to_float(sr[kk / group]) * lut[c]);
+            for (int q = 0; q < cw; ++q) d[q] = (uint8_t)((w >> (bits * q)) & ((1u << bits) - 1u));
+        }
+    }
+    __syncthreads();
+    const int nv = cols / 8;
+    const int ngroups = cols / group;
+    const uint16_t* s0 = scales + (bad ? 0 : (int64_t)e * ess + (int64_t)n0 * ngroups);
+    for (int t = threadIdx.x; t < nr * nv; t += blockDim.x) {
+        const int r = t / nv, v = t - r * nv;
+        const int kk = v * 8;
+        const float sc = bad ? 0.f : half_bits_to_float(__ldg(s0 + (int64_t)r * ngroups + kk / group));
+        const uint2 cb = *reinterpret_cast<const uint2*>(dq + r * cpad + kk);
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = sc * lut[((q < 4 ? cb.x : cb.y) >> (8 * (q & 3))) & 0xffu];
+        const int64_t o = (i_sel * rows + n0 + r) * (int64_t)cols + kk;  // a multiple of 8 elements
+        if (odt == TQ_F32) {
+            float4* y = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+            y[0] = make_float4(f[0], f[1], f[2], f[3]);
+            y[1] = make_float4(f[4], f[5], f[6], f[7]);
+        } else {
+            uint32_t h[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (odt == TQ_BF16) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+                    h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                } else {
+                    const __half2 b2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+                    h[q] = *reinterpret_cast<const uint32_t*>(&b2);
                 }
             }
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
         }
     }
 }
@@ -262,10 +392,16 @@ extern "C" tq_status tq_dequant_experts(const tq_qweight_t* w, const int32_t* id
     if (s != TQ_OK) return s;
     if (n_ids < 0 || !(odt == TQ_F32 || odt == TQ_BF16 || odt == TQ_F16)) return TQ_ERR_INVALID;
     if (n_ids == 0) return TQ_OK;
-    if (!ids || !out || n_ids > 65535) return TQ_ERR_INVALID;
-    dequant_kernel<<<dim3(w->rows, n_ids), 256, 0, as_stream(stream)>>>(
+    if (!ids || !out || n_ids > 65535 || !aligned(out, 16)) return TQ_ERR_INVALID;
+    const int cw = host_codes_per_word(w->cb.levels);
+    const int cpad = (int)((tq_row_words(w->cb.levels, w->cols) * cw + 15) / 16 * 16);
+    if (cpad > 160 * 1024) return TQ_ERR_UNSUPPORTED;
+    const int rpc = std::max(1, std::min(kDqRows, 40960 / cpad));
+    const size_t smem = (size_t)rpc * cpad;
+    if (ensure_smem((const void*)dequant_kernel, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    dequant_kernel<<<dim3((w->rows + rpc - 1) / rpc, n_ids), 256, smem, as_stream(stream)>>>(
         w->codes, w->scales, w->row_stride_words, w->experts > 1 ? w->expert_stride_words : 0,
         w->experts > 1 ? w->expert_stride_scales : 0, w->rows, w->cols, w->group, w->experts, w->cb.centroids,
-        w->cb.levels, ids, out, odt, err);
+        w->cb.levels, ids, out, odt, rpc, cpad, err);
     return launch_status();
 }

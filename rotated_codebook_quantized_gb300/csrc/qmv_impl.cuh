@@ -47,7 +47,10 @@ struct QFmt {
     static_assert(kCB % 4 == 0, "x blocks are whole float4");
 };
 
-enum QmvMode { kModeDense = 0, kModeGather = 1, kModeMulti = 2 };
+// kModeGroups: multi-gather with the pairs grouped by expert; item g is record g of `groups`
+// (groups[0] = number of records; record g at groups + 2 + g * (1 + NV) = expert, then up to NV
+// pair indices, -1 where empty), so each expert's weights are decoded once for all its pairs.
+enum QmvMode { kModeDense = 0, kModeGather = 1, kModeMulti = 2, kModeGroups = 3 };
 
 struct QmvParams {
     const uint32_t* codes;
@@ -68,6 +71,7 @@ struct QmvParams {
     int kpad;        // padded x length in shared memory (multiple of the step)
     int gpad;        // padded group count
     int nsteps;      // steps per row
+    const int32_t* groups;  // kModeGroups: the expert records
 };
 
 TQ_DEVFN uint4 ldg_u4(const uint32_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
@@ -93,7 +97,17 @@ __global__ void __launch_bounds__(256) qmv_kernel(const QmvParams p) {
 
     int e, vec0, nv;
     int64_t out0, out_stride;
-    if (p.mode == kModeDense) {
+    const int32_t* glist = nullptr;  // kModeGroups: this item's pair indices
+    if (p.mode == kModeGroups) {
+        if (item >= __ldg(p.groups)) return;  // uniform: fewer records than the launch's bound
+        const int32_t* rec = p.groups + 2 + (int64_t)item * (1 + NV);
+        e = __ldg(rec);
+        glist = rec + 1;
+        vec0 = 0;
+        nv = NV;
+        out0 = 0;
+        out_stride = 0;
+    } else if (p.mode == kModeDense) {
         e = 0;
         vec0 = item * NV;
         nv = min(NV, p.T - vec0);
@@ -114,6 +128,7 @@ __global__ void __launch_bounds__(256) qmv_kernel(const QmvParams p) {
     }
     if (e < 0 || e >= p.experts) {  // uniform over the CTA
         if (threadIdx.x == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
+        if (glist) return;  // records hold valid experts only; nothing to write here
         for (int i = threadIdx.x; i < 32 * nv; i += blockDim.x) {
             const int r = blockIdx.x * 32 + (i & 31);
             if (r < p.rows) store_from_float(p.y, out0 + (i >> 5) * out_stride + r, p.ydt, 0.f);
@@ -137,9 +152,12 @@ __global__ void __launch_bounds__(256) qmv_kernel(const QmvParams p) {
     if (s0 < s1) load_step(cur, s0);  // first weight bytes in flight before the x fill
 
     // Rotated input (zero padded), per-group input sums (ternary) and the codebook.
+    int vidx[NV];  // input / output row of each vector (-1: none)
+#pragma unroll
+    for (int v = 0; v < NV; ++v) vidx[v] = glist ? __ldg(glist + v) : (v < nv ? vec0 + v : -1);
     for (int v = 0; v < NV; ++v) {
-        const bool has = v < nv;
-        const float* xv = p.x + (int64_t)(vec0 + v) * p.cols;
+        const bool has = vidx[v] >= 0;
+        const float* xv = p.x + (int64_t)(has ? vidx[v] : 0) * p.cols;
         for (int i = threadIdx.x; i < p.kpad; i += blockDim.x) xs[v * p.kpad + i] = (has && i < p.cols) ? xv[i] : 0.f;
     }
     if (threadIdx.x < 16) lut[threadIdx.x] = threadIdx.x < LEVELS ? p.centroids[threadIdx.x] : 0.f;
@@ -248,7 +266,12 @@ __global__ void __launch_bounds__(256) qmv_kernel(const QmvParams p) {
         float sum = 0.f;
         for (int w = 0; w < nwarps; ++w) sum += red[(w * NV + v) * 32 + l];
         const int r = blockIdx.x * 32 + l;
-        if (r < p.rows && v < nv) store_from_float(p.y, out0 + (int64_t)v * out_stride + r, p.ydt, sum);
+        if (glist) {
+            const int pv = __ldg(glist + v);
+            if (r < p.rows && pv >= 0) store_from_float(p.y, (int64_t)pv * p.rows + r, p.ydt, sum);
+        } else if (r < p.rows && v < nv) {
+            store_from_float(p.y, out0 + (int64_t)v * out_stride + r, p.ydt, sum);
+        }
     }
 }
 

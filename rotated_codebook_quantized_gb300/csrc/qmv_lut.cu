@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams l
     int16_t* xq = reinterpret_cast<int16_t*>(sm + kOffXq);
     float* xsg = reinterpret_cast<float*>(sm + kOffXs);
 
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the slice sum may launch (it waits for us)
+    pdl_trigger();  // the slice sum (or the next call) may launch; it waits for this grid
+    pdl_wait();     // ids, x, y and the scratch may belong to the kernel before
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x / lp.cta_per_slice, cb = blockIdx.x - slice * lp.cta_per_slice;
     const int rt_n = lp.row_tasks, n_items = lp.n_items;
@@ -388,7 +389,8 @@ __global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams l
 // y[i] = sum over slices of part[s][i], in slice order.
 __global__ void __launch_bounds__(256) lut_slice_sum_kernel(const float* __restrict__ part, int nslices, int64_t n,
                                                             void* y, int ydt) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         float v = 0.f;
         for (int s = 0; s < nslices; ++s) v += part[s * n + i];
@@ -439,8 +441,7 @@ tq_status qmv_lut_run(const QmvParams& qp, int n_items, void* ws, size_t ws_byte
     lp.cta_per_slice = (int)std::max<int64_t>(1, std::min<int64_t>(sms / lp.nslices, (ntasks + 1) / 2));
     const int grid = lp.cta_per_slice * lp.nslices;
     if (ensure_smem((const void*)qmv_lut_kernel, kLSmem) != cudaSuccess) return TQ_ERR_CUDA;
-    qmv_lut_kernel<<<grid, kLThreads, kLSmem, st>>>(lp);
-    tq_status s = launch_status();
+    tq_status s = launch_pdl(qmv_lut_kernel, dim3(grid), dim3(kLThreads), kLSmem, st, lp);
     if (s != TQ_OK || lp.nslices == 1) return s;
     // the slices' partial sums: a programmatic dependent of the matvec, so its launch overlaps
     const int64_t n = (int64_t)n_items * qp.rows;

@@ -34,6 +34,8 @@ template <int E, class Load>
 __global__ void __launch_bounds__(1024) rotate_rows_kernel(Load ld, int dim, int span, int block, float scale,
                                                            const int8_t* __restrict__ signs, void* out, int odt) {
     extern __shared__ float s[];
+    pdl_trigger();
+    pdl_wait();
     const int spans = dim / span;
     const int64_t row = blockIdx.x / spans;
     const int base = (blockIdx.x - (int)(row * spans)) * span + threadIdx.x * E;
@@ -101,8 +103,8 @@ tq_status launch_rotate(const Load& ld, int64_t rows, const tq_rotation_t* rot, 
 #define TQ_ROT_CASE(EE)                                                                                   \
     case EE:                                                                                              \
         if (ensure_smem((const void*)rotate_rows_kernel<EE, Load>, smem) != cudaSuccess) return TQ_ERR_CUDA; \
-        rotate_rows_kernel<EE, Load><<<grid, threads, smem, st>>>(ld, dim, span, block, scale, rot->signs, out, odt); \
-        break;
+        return launch_pdl(rotate_rows_kernel<EE, Load>, grid, dim3(threads), smem, st, ld, dim, span, block, scale, \
+                          rot->signs, out, (int)odt);
         TQ_ROT_CASE(1)
         TQ_ROT_CASE(2)
         TQ_ROT_CASE(4)

@@ -104,6 +104,9 @@ def test_multi_gather_qmv_bitpacked(lib, levels, group, K, rows):
     ref = o.multi_gather_qmv(Wh, ids, x)
     assert rel_l2(y, ref) < BITS_TOL
     assert lib.check_error(err) == 0
+    # pairs grouped by expert (each expert decoded once) give the per-pair kernel's bits
+    ypp = lib.multi_gather_qmv(qw, _dev(x), _dev(ids), use_ws=False).cpu().numpy()
+    np.testing.assert_array_equal(y, ypp)
     bad = ids.copy()
     bad[4] = 99
     y = lib.multi_gather_qmv(qw, _dev(x), _dev(bad), err=err).cpu().numpy()
@@ -111,6 +114,21 @@ def test_multi_gather_qmv_bitpacked(lib, levels, group, K, rows):
     assert np.all(y[4] == 0)
     keep = np.arange(len(ids)) != 4
     assert rel_l2(y[keep], ref[keep]) < BITS_TOL
+
+
+def test_multi_gather_qmv_grouped_prefill_shape(lib):
+    """8 tokens x top-8 of 128 experts under a Zipf(1.1) router (64 pairs, many repeats), 3-bit
+    group 64 over K = 1536: every pair against the oracle, and equal to the per-pair kernel."""
+    E, K, rows, T, k = 128, 1536, 256, 8, 8
+    qw, Wh = _bank(lib, 8, E, rows, K, 64, seed=77)
+    logits = wl.router_logits(77, T, E, zipf=1.1)
+    oids, _ = o.route(logits, k)
+    ids = oids.reshape(-1).astype(np.int32)
+    assert len(set(ids.tolist())) < len(ids)
+    x = wl.rng(77, 3).normal(size=(T * k, K)).astype(np.float32)
+    y = lib.multi_gather_qmv(qw, _dev(x), _dev(ids)).cpu().numpy()
+    assert rel_l2(y, o.multi_gather_qmv(Wh, ids, x)) < BITS_TOL
+    np.testing.assert_array_equal(y, lib.multi_gather_qmv(qw, _dev(x), _dev(ids), use_ws=False).cpu().numpy())
 
 
 def test_multi_gather_qmv_ternary_repeats_and_bad_id(lib):
@@ -196,3 +214,17 @@ def test_dequant_experts_bf16_ternary_and_bad_id(lib):
     assert lib.check_error(err) == lib.TQ_DEVERR_BAD_ID
     assert not np.any(outb[1]) and not np.any(outb[2])
     np.testing.assert_allclose(outb[[0, 3]], o.dequant_experts(Wh, np.array([1, 2])), rtol=2.0 ** -8, atol=0)
+
+
+@pytest.mark.parametrize("levels,group,rows,K,odt", [(4, 16, 37, 1024, "f32"), (16, 32, 13, 2080, "f16"),
+                                                     (3, 16, 9, 7168, "bf16"), (8, 128, 6, 23040, "f32")])
+def test_dequant_experts_books_and_ragged_rows(lib, levels, group, rows, K, odt):
+    """2- and 4-bit books, rows that do not fill the last run of a CTA, a code row wider than one CTA's
+    staging of several rows (K = 23040 takes one row per CTA), each output type."""
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[odt]
+    qw, Wh = _bank(lib, levels, 3, rows, K, group, seed=70 + levels)
+    ids = np.array([2, 0, 2, 1], dtype=np.int32)
+    out = lib.dequant_experts(qw, _dev(ids), out_dtype=dt).float().cpu().numpy()
+    ref = o.dequant_experts(Wh, ids)
+    tol = {"f32": 1e-6, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}[odt]
+    np.testing.assert_allclose(out, ref, rtol=tol, atol=1e-12 if odt == "f32" else 1e-7)
