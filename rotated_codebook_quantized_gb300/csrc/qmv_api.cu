@@ -105,6 +105,10 @@ extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T
     // Bit-packed books at small T take the staged kernel, one vector per item (later vectors
     // re-read the weights, mostly from L2).  From T = 16 on, the batched kernel below, which
     // decodes each weight once for up to 4 vectors, is faster (295 vs 268 us at 11008x4096).
+    if (T <= 8 && qmv_rows_ok(p, w->group)) {
+        const tq_status rs = qmv_rows_run(p, w->group, T, nullptr, 0, as_stream(stream));
+        if (rs != TQ_ERR_UNSUPPORTED) return rs;
+    }
     if (T <= 8 && qmv_bits_ok(p, w->group)) return qmv_bits_run(p, w->group, T, as_stream(stream));
     const int nv = pick_nv(T, host_kpad(w->cb.levels, w->group, w->cols));
     return run(p, w->group, nv, (T + nv - 1) / nv, as_stream(stream));
@@ -112,7 +116,8 @@ extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T
 
 namespace {
 
-// The table-lookup kernel when it applies and its scratch is there; else the single-pass kernels.
+// The table-lookup kernel (three-level books) or the row-per-lane kernel (bit-packed books) when
+// it applies and its scratch is there; else the single-pass kernels.
 tq_status run_items(const QmvParams& p, int group, int n_items, void* ws, size_t ws_bytes, cudaStream_t st) {
     if (qmv_lut_ok(p, group)) {
         const size_t need = qmv_lut_workspace_bytes(p.cols, n_items, p.rows);
@@ -121,46 +126,66 @@ tq_status run_items(const QmvParams& p, int group, int n_items, void* ws, size_t
             if (s != TQ_ERR_UNSUPPORTED) return s;
         }
     }
+    if (qmv_rows_ok(p, group)) {
+        const size_t need = qmv_rows_workspace_bytes(p.levels, group, p.cols, n_items, p.rows);
+        if (need == 0 || (ws && ws_bytes >= need && aligned(ws, 16))) {
+            const tq_status s = qmv_rows_run(p, group, n_items, ws, ws_bytes, st);
+            if (s != TQ_ERR_UNSUPPORTED) return s;
+        }
+    }
     return run(p, group, 1, n_items, st);
 }
 
 size_t items_workspace(const tq_qweight_t* w, int64_t n_items) {
-    if (!w || w->cb.levels != 3 || w->group != 16 || w->rows <= 0 || w->cols <= 0 || n_items <= 0) return 0;
-    return qmv_lut_workspace_bytes(w->cols, n_items, w->rows);
+    if (!w || w->rows <= 0 || w->cols <= 0 || n_items <= 0) return 0;
+    if (w->cb.levels == 3) return w->group == 16 ? qmv_lut_workspace_bytes(w->cols, n_items, w->rows) : 0;
+    return qmv_rows_workspace_bytes(w->cb.levels, w->group, w->cols, n_items, w->rows);
 }
 
 }  // namespace
 
 namespace {
 
-// Multi-gather of bit-packed books, pairs grouped by expert: a record holds an expert and up to
-// kGroupNV of its pairs, and the matvec decodes each record's weights once for all of them.
-constexpr int kGroupNV = 4;
+// Multi-gather of bit-packed books, pairs grouped by expert.  An expert with c pairs gets
+// c / 4 records of four pairs and its remainder as one record of 3, 2 or 1 pairs; records of
+// three or four pairs, of two and of one go to three lists, each run by the matvec instance
+// with as many input vectors (4, 2, 1), so each expert's weights are decoded once per record
+// and no instance multiplies empty vector slots beyond a record of three.
+constexpr int kListNV[3] = {4, 2, 1};
 
 bool groups_apply(const tq_qweight_t* w, int64_t P) {
     return w && (w->cb.levels == 4 || w->cb.levels == 8 || w->cb.levels == 16) && P >= 2 && w->experts >= 1 &&
-           w->experts <= (1 << 20);
+           w->experts <= (1 << 20) && P <= (1 << 26);
 }
 
-// Workspace of the grouping: records (2 + P * (1 + NV) ints), then per expert its pair count,
-// fill counter and first record (3 * experts ints).
+// Most records list i can hold, and its size in ints (a count, a pad, then the records).
+int64_t list_cap(int i, int64_t P) { return i == 0 ? (P + 2) / 3 : (i == 1 ? P / 2 : P); }
+int64_t list_ints(int i, int64_t P) { return 2 + list_cap(i, P) * (1 + kListNV[i]); }
+
+// Workspace of the grouping: the three record lists, then per expert its pair count, fill
+// counter and first record in each list (5 * experts ints).
 size_t groups_workspace(const tq_qweight_t* w, int64_t P) {
     if (!groups_apply(w, P)) return 0;
-    return ((size_t)(2 + P * (1 + kGroupNV)) + 3 * (size_t)w->experts) * 4 + 16;
+    int64_t ints = 5 * (int64_t)w->experts;
+    for (int i = 0; i < 3; ++i) ints += list_ints(i, P);
+    return (size_t)ints * 4 + 16;
 }
 
-// One CTA: count the pairs of each expert, lay out each expert's records (experts in ascending
-// order), then place every pair in a slot of its expert's records.  The slot order within an
+struct GroupLists {
+    int32_t* list[3];
+};
+
+// One CTA: count each expert's pairs, lay out its records (experts in ascending order in each
+// list), then place every pair in a slot of a record of its expert.  The slot order within an
 // expert follows atomics, which changes nothing in the results (each pair's sums are its own).
 // A pair whose id is outside the bank gets a zero output row and raises BAD_ID.
 __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                                           int32_t* __restrict__ groups, int32_t* __restrict__ cnt,
-                                                           void* y, int rows, int ydt, uint32_t* err) {
-    constexpr int NV = kGroupNV;
-    __shared__ int part[1024];
+                                                           GroupLists L, int32_t* __restrict__ cnt, void* y,
+                                                           int rows, int ydt, uint32_t* err) {
+    __shared__ int part[3][1024];
     __shared__ int any_bad;
     int32_t* fill = cnt + E;
-    int32_t* first = fill + E;
+    int32_t* first = fill + E;  // [3][E]
     const int tid = threadIdx.x, nt = blockDim.x;
     if (tid == 0) any_bad = 0;
     for (int e = tid; e < E; e += nt) cnt[e] = fill[e] = 0;
@@ -171,38 +196,57 @@ __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __rest
         else any_bad = 1;
     }
     __syncthreads();
-    // records per expert, exclusive prefix over the experts (a contiguous range per thread)
+    // records of each expert in each list: four-slot list c/4 + (c%4 == 3), two-slot c%4 == 2,
+    // one-slot c%4 == 1; exclusive prefixes over the experts (a contiguous range per thread)
+    auto nrec = [](int c, int i) { return i == 0 ? c / 4 + (c % 4 == 3) : (i == 1 ? (c % 4 == 2) : (c % 4 == 1)); };
     const int per = (E + nt - 1) / nt, e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    int local = 0;
-    for (int e = e0; e < e1; ++e) local += (cnt[e] + NV - 1) / NV;
-    part[tid] = local;
+    for (int i = 0; i < 3; ++i) {
+        int local = 0;
+        for (int e = e0; e < e1; ++e) local += nrec(cnt[e], i);
+        part[i][tid] = local;
+    }
     __syncthreads();
-    if (tid == 0) {
+    if (tid < 3) {
         int acc = 0;
         for (int t = 0; t < nt; ++t) {
-            const int v = part[t];
-            part[t] = acc;
+            const int v = part[tid][t];
+            part[tid][t] = acc;
             acc += v;
         }
-        groups[0] = acc;
-        groups[1] = 0;
+        L.list[tid][0] = acc;
+        L.list[tid][1] = 0;
     }
     __syncthreads();
-    int run = part[tid];
-    for (int e = e0; e < e1; ++e) {
-        first[e] = run;
-        run += (cnt[e] + NV - 1) / NV;
+    for (int i = 0; i < 3; ++i) {
+        int run = part[i][tid];
+        for (int e = e0; e < e1; ++e) {
+            first[i * E + e] = run;
+            run += nrec(cnt[e], i);
+        }
     }
-    const int ng = groups[0];
-    for (int i = tid; i < ng * NV; i += nt) groups[2 + (i / NV) * (1 + NV) + 1 + i % NV] = -1;
+    for (int i = 0; i < 3; ++i) {
+        const int nv = i == 0 ? 4 : (i == 1 ? 2 : 1), nr = L.list[i][0];
+        for (int j = tid; j < nr * nv; j += nt) L.list[i][2 + (j / nv) * (1 + nv) + 1 + j % nv] = -1;
+    }
     __syncthreads();
     for (int i = tid; i < P; i += nt) {
         const int e = __ldg(ids + i);
         if (e < 0 || e >= E) continue;
-        const int slot = atomicAdd(fill + e, 1);
-        int32_t* rec = groups + 2 + (int64_t)(first[e] + slot / NV) * (1 + NV);
-        rec[0] = e;
-        rec[1 + slot % NV] = i;
+        const int c = cnt[e], q = c / 4, slot = atomicAdd(fill + e, 1);
+        int li, rec, pos;
+        if (slot < 4 * q || c % 4 == 3) {
+            li = 0;
+            rec = first[e] + slot / 4;
+            pos = slot % 4;
+        } else {
+            li = c % 4 == 2 ? 1 : 2;
+            rec = first[li * E + e];
+            pos = slot - 4 * q;
+        }
+        const int nv = li == 0 ? 4 : (li == 1 ? 2 : 1);
+        int32_t* r = L.list[li] + 2 + (int64_t)rec * (1 + nv);
+        r[0] = e;
+        r[1 + pos] = i;
     }
     if (!any_bad) return;  // uniform
     if (tid == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
@@ -214,16 +258,24 @@ __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __rest
 }
 
 tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaStream_t st) {
-    uint8_t* b = static_cast<uint8_t*>(ws);
-    int32_t* groups = reinterpret_cast<int32_t*>(b);
-    int32_t* cnt = groups + 2 + (size_t)P * (1 + kGroupNV);
-    group_pairs_kernel<<<1, 1024, 0, st>>>(p.ids, P, w->experts, groups, cnt, p.y, p.rows, p.ydt, p.err);
+    int32_t* base = static_cast<int32_t*>(ws);
+    GroupLists L;
+    int64_t off = 0;
+    for (int i = 0; i < 3; ++i) {
+        L.list[i] = base + off;
+        off += list_ints(i, P);
+    }
+    int32_t* cnt = base + off;
+    group_pairs_kernel<<<1, 1024, 0, st>>>(p.ids, P, w->experts, L, cnt, p.y, p.rows, p.ydt, p.err);
     tq_status s = launch_status();
     if (s != TQ_OK) return s;
     p.mode = kModeGroups;
-    p.groups = groups;
-    // at most P records (one per pair); launches past the actual count return at once
-    return run(p, w->group, kGroupNV, P, st);
+    for (int i = 0; i < 3; ++i) {  // each launch has room for the list's most records; the rest return at once
+        p.groups = L.list[i];
+        s = run(p, w->group, kListNV[i], (int)std::max<int64_t>(1, list_cap(i, P)), st);
+        if (s != TQ_OK) return s;
+    }
+    return TQ_OK;
 }
 
 }  // namespace
@@ -266,7 +318,7 @@ extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_r
     p.ids = ids;
     p.k = 1;
     const size_t gneed = groups_workspace(w, P);
-    if (gneed > 0 && ws && ws_bytes >= gneed && aligned(ws, 16))
+    if (!qmv_rows_ok(p, w->group) && gneed > 0 && ws && ws_bytes >= gneed && aligned(ws, 16))
         return run_groups(p, w, P, ws, as_stream(stream));
     return run_items(p, w->group, P, ws, ws_bytes, as_stream(stream));
 }
@@ -316,72 +368,89 @@ namespace {
 // writes 512 contiguous bytes per instruction.
 constexpr int kDqRows = 4;
 
+template <int LEVELS>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ codes,
                                                       const uint16_t* __restrict__ scales, int64_t row_stride,
-                                                      int64_t esw, int64_t ess, int rows, int cols, int group,
-                                                      int experts, const float* __restrict__ centroids, int levels,
+                                                      int64_t esw, int64_t ess, int rows, int cols, int gshift,
+                                                      int experts, const float* __restrict__ centroids,
                                                       const int32_t* __restrict__ ids, void* out, int odt, int rpc,
                                                       int cpad, uint32_t* err) {
+    constexpr int BITS = LEVELS == 3 ? 0 : (LEVELS == 2 ? 1 : (LEVELS == 4 ? 2 : (LEVELS == 8 ? 3 : (LEVELS == 16 ? 4 : 8))));
+    constexpr int CW = LEVELS == 3 ? 20 : (LEVELS == 8 ? 10 : 32 / BITS);
     extern __shared__ __align__(16) uint8_t dq[];  // [rpc][cpad] code bytes
-    __shared__ float lut[256];
-    for (int i = threadIdx.x; i < levels; i += blockDim.x) lut[i] = centroids[i];
+    __shared__ float lut[LEVELS];
+    for (int i = threadIdx.x; i < LEVELS; i += blockDim.x) lut[i] = centroids[i];
     const int n0 = blockIdx.x * rpc;
     const int nr = min(rpc, rows - n0);
     const int64_t i_sel = blockIdx.y;
     const int e = ids[i_sel];
     const bool bad = e < 0 || e >= experts;
     if (bad && threadIdx.x == 0 && err) atomicOr(err, TQ_DEVERR_BAD_ID);
-    const int cw = levels == 3 ? 20 : (levels == 8 ? 10 : 32 / (31 - __clz(levels)));
-    const int bits = 31 - __clz(levels);
-    const int nw = (cols + cw - 1) / cw;
+    const int nw = (cols + CW - 1) / CW;
     const uint32_t* w0 = codes + (bad ? 0 : (int64_t)e * esw + (int64_t)n0 * row_stride);
-    for (int t = threadIdx.x; t < nr * nw; t += blockDim.x) {
-        const int r = t / nw, j = t - r * nw;
-        const uint32_t w = bad ? 0u : __ldg(w0 + (int64_t)r * row_stride + j);
-        uint8_t* d = dq + r * cpad + j * cw;  // cpad >= nw * cw: the tail of the last word lands in padding
-        if (levels == 3) {
-            const TritHalves th = trit_split(w);
-            uint32_t Fh = th.hi, Fl = th.lo;
+    for (int r = 0; r < nr; ++r) {
+        for (int j = threadIdx.x; j < nw; j += blockDim.x) {
+            const uint32_t w = bad ? 0u : __ldg(w0 + (int64_t)r * row_stride + j);
+            uint8_t* d = dq + r * cpad + j * CW;  // cpad >= nw * CW: the last word's tail lands in padding
+            if constexpr (LEVELS == 3) {
+                const TritHalves th = trit_split(w);
+                uint32_t Fh = th.hi, Fl = th.lo;
 #pragma unroll
-            for (int q = 0; q < 10; ++q) d[19 - q] = (uint8_t)trit_next_int(Fh);
+                for (int q = 0; q < 10; ++q) d[19 - q] = (uint8_t)trit_next_int(Fh);
 #pragma unroll
-            for (int q = 0; q < 10; ++q) d[9 - q] = (uint8_t)trit_next_int(Fl);
-        } else {
-            for (int q = 0; q < cw; ++q) d[q] = (uint8_t)((w >> (bits * q)) & ((1u << bits) - 1u));
+                for (int q = 0; q < 10; ++q) d[9 - q] = (uint8_t)trit_next_int(Fl);
+            } else {
+#pragma unroll
+                for (int q = 0; q < CW; ++q) d[q] = (uint8_t)((w >> (BITS * q)) & ((1u << BITS) - 1u));
+            }
         }
     }
     __syncthreads();
     const int nv = cols / 8;
-    const int ngroups = cols / group;
+    const int ngroups = cols >> gshift;
     const uint16_t* s0 = scales + (bad ? 0 : (int64_t)e * ess + (int64_t)n0 * ngroups);
-    for (int t = threadIdx.x; t < nr * nv; t += blockDim.x) {
-        const int r = t / nv, v = t - r * nv;
-        const int kk = v * 8;
-        const float sc = bad ? 0.f : half_bits_to_float(__ldg(s0 + (int64_t)r * ngroups + kk / group));
-        const uint2 cb = *reinterpret_cast<const uint2*>(dq + r * cpad + kk);
-        float f[8];
+    for (int r = 0; r < nr; ++r) {
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const int kk = v * 8;
+            const float sc = bad ? 0.f : half_bits_to_float(__ldg(s0 + (int64_t)r * ngroups + (kk >> gshift)));
+            const uint2 cb = *reinterpret_cast<const uint2*>(dq + r * cpad + kk);
+            float f[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = sc * lut[((q < 4 ? cb.x : cb.y) >> (8 * (q & 3))) & 0xffu];
-        const int64_t o = (i_sel * rows + n0 + r) * (int64_t)cols + kk;  // a multiple of 8 elements
-        if (odt == TQ_F32) {
-            float4* y = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
-            y[0] = make_float4(f[0], f[1], f[2], f[3]);
-            y[1] = make_float4(f[4], f[5], f[6], f[7]);
-        } else {
-            uint32_t h[4];
+            for (int q = 0; q < 8; ++q) f[q] = sc * lut[((q < 4 ? cb.x : cb.y) >> (8 * (q & 3))) & 0xffu];
+            const int64_t o = (i_sel * rows + n0 + r) * (int64_t)cols + kk;  // a multiple of 8 elements
+            if (odt == TQ_F32) {
+                float4* y = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+                y[0] = make_float4(f[0], f[1], f[2], f[3]);
+                y[1] = make_float4(f[4], f[5], f[6], f[7]);
+            } else {
+                uint32_t h[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (odt == TQ_BF16) {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
-                    h[q] = *reinterpret_cast<const uint32_t*>(&b2);
-                } else {
-                    const __half2 b2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
-                    h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                for (int q = 0; q < 4; ++q) {
+                    if (odt == TQ_BF16) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+                        h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    } else {
+                        const __half2 b2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+                        h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
                 }
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
             }
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
         }
     }
+}
+
+template <int LEVELS>
+tq_status launch_dequant(const tq_qweight_t* w, const int32_t* ids, int32_t n_ids, void* out, tq_dtype odt,
+                         uint32_t* err, int rpc, int cpad, cudaStream_t st) {
+    const size_t smem = (size_t)rpc * cpad;
+    if (ensure_smem((const void*)dequant_kernel<LEVELS>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    const int gshift = __builtin_ctz((unsigned)w->group);
+    dequant_kernel<LEVELS><<<dim3((w->rows + rpc - 1) / rpc, n_ids), 256, smem, st>>>(
+        w->codes, w->scales, w->row_stride_words, w->experts > 1 ? w->expert_stride_words : 0,
+        w->experts > 1 ? w->expert_stride_scales : 0, w->rows, w->cols, gshift, w->experts, w->cb.centroids, ids, out,
+        (int)odt, rpc, cpad, err);
+    return launch_status();
 }
 
 }  // namespace
@@ -397,11 +466,14 @@ extern "C" tq_status tq_dequant_experts(const tq_qweight_t* w, const int32_t* id
     const int cpad = (int)((tq_row_words(w->cb.levels, w->cols) * cw + 15) / 16 * 16);
     if (cpad > 160 * 1024) return TQ_ERR_UNSUPPORTED;
     const int rpc = std::max(1, std::min(kDqRows, 40960 / cpad));
-    const size_t smem = (size_t)rpc * cpad;
-    if (ensure_smem((const void*)dequant_kernel, smem) != cudaSuccess) return TQ_ERR_CUDA;
-    dequant_kernel<<<dim3((w->rows + rpc - 1) / rpc, n_ids), 256, smem, as_stream(stream)>>>(
-        w->codes, w->scales, w->row_stride_words, w->experts > 1 ? w->expert_stride_words : 0,
-        w->experts > 1 ? w->expert_stride_scales : 0, w->rows, w->cols, w->group, w->experts, w->cb.centroids,
-        w->cb.levels, ids, out, odt, rpc, cpad, err);
-    return launch_status();
+    cudaStream_t st = as_stream(stream);
+    switch (w->cb.levels) {
+        case 2: return launch_dequant<2>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        case 3: return launch_dequant<3>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        case 4: return launch_dequant<4>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        case 8: return launch_dequant<8>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        case 16: return launch_dequant<16>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        case 256: return launch_dequant<256>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
 }

@@ -332,6 +332,12 @@ size_t qmv_lut_workspace_bytes(int cols, int64_t n_items, int rows);
 tq_status qmv_lut_run(const QmvParams& p, int n_items, void* ws, size_t ws_bytes, cudaStream_t st);
 bool qmv_bits_ok(const QmvParams& p, int group);
 tq_status qmv_bits_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
+// Bit-packed books, one matrix row per lane (qmv_rows.cu): every mode but kModeGroups.  Rows
+// longer than one column chunk need qmv_rows_workspace_bytes of scratch for the chunks'
+// partial sums; without it an f32 output is zeroed and the chunks add into it.
+bool qmv_rows_ok(const QmvParams& p, int group);
+size_t qmv_rows_workspace_bytes(int levels, int group, int cols, int64_t n_items, int rows);
+tq_status qmv_rows_run(const QmvParams& p, int group, int n_items, void* ws, size_t ws_bytes, cudaStream_t st);
 
 // One entry point per (levels, group), each compiled in its own translation unit.
 #define TQ_QMV_DECL(L, G) tq_status qmv_run_l##L##_g##G(QmvParams p, int nv, int n_items, cudaStream_t st);
