@@ -517,7 +517,7 @@ def measure_streaming(torch, tq, wl, dev, qgu, steps=32):
     return out
 
 
-CASES = ("gate_up", "down", "dense_t1", "multi_t8", "dequant", "quantize", "kv_quantize", "kv_attend")
+CASES = ("gate_up", "down", "dense_t1", "multi_t8", "dequant", "quantize", "kv_quantize", "kv_attend", "prefill_gate_up")
 
 
 def run_case(name: str):
@@ -564,6 +564,13 @@ def run_case(name: str):
             for i in range(3):
                 ids = torch.tensor([(7 + 13 * j + 8 * i) % P_E for j in range(8)], dtype=torch.int32, device=dev)
                 out = tq.dequant_experts(qp, ids, out_dtype=torch.bfloat16)
+    elif name == "prefill_gate_up":  # 4096 tokens top-8 of 128 experts (Zipf), 3-bit [3072, 4096] group 64
+        qgu = random_bit_bank(torch, tq, dev, gen, P_E, 2 * P_I, P_H, 8, P_G)
+        logits = torch.from_numpy(wl.router_logits(P_SEED, P_T, P_E, zipf=1.1)).to(dev)
+        ids, probs, perm, pos, off = tq.moe_route(logits, P_K)
+        x = torch.randn((P_T, P_H), generator=gen, device=dev).half()
+        for _ in range(2):
+            out = tq.gather_qmm(qgu, x, perm, off, P_K, out_dtype=torch.bfloat16)
     elif name == "quantize":  # two 11008 x 4096 bf16 inputs in turn (180 MB)
         Ws = [(torch.randn((11008, 4096), generator=gen, device=dev) * 0.02).to(torch.bfloat16) for _ in range(2)]
         rot = tq.Rotation(4096, 4096, seed=11, device=dev)

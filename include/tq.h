@@ -518,7 +518,9 @@ tq_status tq_expert_cache_stats(const tq_expert_cache* cache, int64_t* hits, int
 tq_status tq_check_error(uint32_t* err, uint32_t* bits, void* stream);
 
 /* Test hook for the bounded waits of the tensor-core kernels (tq_gather_qmm,
- * tq_qmv_tc): every wait of a pipeline role on another (an mbarrier phase)
+ * tq_qmv_tc) and of the three-level tensor-copy matvec (the ternary kernel of
+ * calls without scratch, of groups other than 16 and of the fused input
+ * stages): every wait of a pipeline role on another (an mbarrier phase)
  * gives up after `cycles` SM clock cycles, raises TQ_DEVERR_TIMEOUT in the
  * call's error word (tq_check_error then returns TQ_ERR_TIMEOUT) and the CTA
  * stops: each role drains the copies and MMAs it has in flight (bounded by the

@@ -753,10 +753,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (warp < kMmaWarps) {
         // ------------------------------------------------ MMA issuers (one thread each)
         // Each MMA instruction blocks its thread for tens of cycles and each commit for about a
-        // hundred, so two threads share a tile: with at most 128 pairs they take alternate
-        // K stages into their own 128 accumulator columns (the epilogue adds the two); with
-        // more, thread 0 computes pair columns 0..127 and thread 1 the rest.  Both wait for
-        // every stage and commit every stage, so a slot is released only after both.
+        // hundred, so two threads share a tile of at most 128 pairs: they take alternate K
+        // stages into their own 128 accumulator columns (the epilogue adds the two).  A wider
+        // tile is one N = 256 MMA per K step from thread 0 (the tensor pipe runs at full rate
+        // only at N = 256), thread 1 only committing.  Both wait for every stage and commit
+        // every stage, so a slot is released only after both.
         if (lane == 0) {
             const int me = warp;
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -767,13 +768,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const int kb = I.kb, ke = I.ke;
                 const int ninst = (I.nvalid + 15) & ~15;
                 const bool ksplit = ninst <= 128 && ke - kb >= 2;
-                const int ncols = ksplit ? ninst : (me == 0 ? min(ninst, 128) : ninst - 128);
+                const int ncols = ksplit ? ninst : (me == 0 ? ninst : 0);
                 const uint32_t idesc = f16_idesc(XT, ncols > 0 ? ncols : 16);
                 const int buf = tile_it & 1;
                 if (!mbar_wait(tile_empty + buf, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * kBuf + me * kHalf);
-                const uint32_t boff = ksplit ? 0u : (uint32_t)(me * 128 * 128);  // B rows of thread 1's columns
+                const uint32_t boff = 0u;
                 for (int kc = kb; kc < ke; ++kc, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(full + s, (it / kStages) & 1, abort_flag, p.wait_cycles)) {

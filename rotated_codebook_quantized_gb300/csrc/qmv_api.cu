@@ -60,6 +60,7 @@ QmvParams make_params(const tq_qweight_t* w, const float* x, void* y, tq_dtype y
     p.y = y;
     p.ydt = ydt;
     p.err = err;
+    p.wait_cycles = wait_budget();
     return p;
 }
 

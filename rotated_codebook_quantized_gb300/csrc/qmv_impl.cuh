@@ -72,6 +72,7 @@ struct QmvParams {
     int gpad;        // padded group count
     int nsteps;      // steps per row
     const int32_t* groups;  // kModeGroups: the expert records
+    long long wait_cycles = 1ll << 31;  // budget of each bounded wait of the tensor-copy kernel
 };
 
 TQ_DEVFN uint4 ldg_u4(const uint32_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }

@@ -978,7 +978,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
                     t0 = clock64();
                 } else {
                     if (*abort_flag) break;
-                    if (clock64() - t0 > kWaitCycles) {
+                    if (clock64() - t0 > p.wait_cycles) {
                         *abort_flag = 1;
                         break;
                     }
@@ -1213,7 +1213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) qmv_trit_tc_kernel(const TritPa
             constexpr bool OFF = decltype(off_c)::value;
             uint32_t slot = cw * D + uses % D, par = (uses / D) & 1;
             for (;;) {
-                if (!mbar_wait_short(full + slot, par, abort_flag)) break;
+                if (!mbar_wait_short(full + slot, par, abort_flag, p.wait_cycles)) break;
                 const int tg = tag[slot];
                 if (tg < 0) {  // end of the segment
                     __syncwarp();

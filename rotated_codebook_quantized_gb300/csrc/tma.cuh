@@ -84,12 +84,13 @@ TQ_DEVFN bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, 
 
 // The same bounded wait, polling with short sleeps (for waits expected to be brief, where a
 // long suspension would outlast the event).
-TQ_DEVFN bool mbar_wait_short(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+TQ_DEVFN bool mbar_wait_short(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                               long long budget = kWaitCycles) {
     if (mbar_test(b, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test(b, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }

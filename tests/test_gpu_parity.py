@@ -310,6 +310,19 @@ def test_route(lib, T, E, k, zipf):
     np.testing.assert_allclose(probs2.cpu().numpy(), oprobs, rtol=2e-6, atol=1e-7)
 
 
+def test_route_signed_zero_ties(lib):
+    """-0.0 and +0.0 are one value: the tie goes to the lower expert id whatever the sign bits."""
+    E, k = 64, 6
+    logits = np.full((2, E), -1.0, np.float32)
+    logits[0, [3, 9, 20, 41, 50, 63]] = [-0.0, 0.0, -0.0, 0.0, -0.0, 0.0]
+    logits[1, [5, 6]] = [0.0, -0.0]
+    logits[1, [30, 31, 32, 33]] = 0.5
+    ids, probs, _, _, _ = lib.moe_route(_dev(logits), k, sort=False)
+    oids, oprobs = o.route(logits, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(probs.cpu().numpy(), oprobs, rtol=2e-6, atol=1e-7)
+
+
 def test_swiglu_rotate_and_combine(lib):
     P, inter = 19, 1536
     gu = wl.rng(10).normal(size=(P, 2 * inter)).astype(np.float32)

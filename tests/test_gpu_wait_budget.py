@@ -63,6 +63,34 @@ def test_qmv_tc_wait_budget_zero(lib):
     torch.testing.assert_close(again, good, rtol=1e-5, atol=1e-6)  # split-K partial sums: any order
 
 
+def test_ternary_tensor_copy_matvec_wait_budget_zero(lib):
+    """The ternary tensor-copy matvec (tq_gather_qmv_rotate: the input rotation in its prologue,
+    then a producer warp feeding 15 decoder warps through mbarrier rings), with enough stages per
+    decoder (8 experts x 4096 rows x 7168 columns) that producer and decoders wait on each other:
+    at budget 0 the waits give up and the call reports TQ_ERR_TIMEOUT; the next call at the default
+    budget gives the earlier result."""
+    from tests.test_gpu_coverage import _random_bank
+
+    E, rows, K, T, k = 8, 4096, 7168, 1, 8
+    words, scales = _random_bank(3, E, rows, K, 16, seed=64)
+    cb = lib.Codebook(3)
+    qw = lib.QWeight(_dev(words.view(np.int32)), _dev(scales.view(np.int16)), E, rows, K, 16, cb,
+                     row_stride=words.shape[-1])
+    rot = lib.Rotation(K, 1024, seed=64)
+    ids = np.array([[4, 0, 5, 2, 7, 1, 6, 3]], dtype=np.int32)
+    x = np.random.default_rng(64).normal(size=(T, K)).astype(np.float32)
+    xd, idd = _dev(x), _dev(ids)
+    good = lib.gather_qmv_rotate(qw, xd, rot, idd)
+    torch.cuda.synchronize()
+    st, bits = _expire(lib, lambda err: lib.gather_qmv_rotate(qw, xd, rot, idd, err=err))
+    assert st == lib.TQ_ERR_TIMEOUT and bits & lib.TQ_DEVERR_TIMEOUT, (st, bits)
+    for _ in range(2):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        again = lib.gather_qmv_rotate(qw, xd, rot, idd, err=err)
+        assert lib.check_error(err) == 0
+        torch.testing.assert_close(again, good, rtol=1e-5, atol=1e-6 * float(good.abs().max()))  # atomics
+
+
 def test_wait_budget_default_is_restored(lib):
     """With the default budget a long gather-GEMM raises nothing."""
     levels, group, E, rows, K, T, k = 8, 64, 8, 512, 2048, 256, 4
