@@ -501,10 +501,13 @@ void tq_expert_cache_destroy(tq_expert_cache* cache);
  * than slots not used by the step (no slot changes content). */
 tq_status tq_expert_cache_plan(tq_expert_cache* cache, const int32_t* ids, int32_t n, int32_t* slots, uint8_t* miss);
 
-/* tq_expert_cache_plan, then for every miss two cudaMemcpyAsync host-to-device
- * copies on `stream` (the expert's code words, then its scales) into its slot.
- * Work on `stream` after the call sees the experts in place.  TQ_ERR_CUDA if a
- * copy cannot be enqueued. */
+/* tq_expert_cache_plan, then the copies of every missing expert's code words
+ * and scales into its slot, on `stream`: one kernel launch that reads the bank
+ * directly over the CPU-GPU link when the bank is pinned memory mapped into the
+ * device's address space and every expert's codes and scales are whole 16-byte
+ * pieces at 16-byte aligned addresses (checked at creation), else two
+ * cudaMemcpyAsync per missing expert.  Work on `stream` after the call sees the
+ * experts in place.  TQ_ERR_CUDA if a copy cannot be enqueued. */
 tq_status tq_expert_cache_map(tq_expert_cache* cache, const int32_t* ids, int32_t n, int32_t* slots, void* stream);
 
 /* Counters since creation: distinct-per-step hits and misses, and bytes copied

@@ -30,6 +30,7 @@ struct tq_expert_cache {
     std::vector<int64_t> last_use;  // step of each slot's last use (0: never)
     std::vector<int> expert_slot;   // slot of each expert, -1 if not cached
     std::vector<int64_t> seen;      // step in which each expert was last looked up
+    bool kernel_copy = false;       // the bank is pinned, mapped and 16-byte aligned: copied by a kernel
     int64_t step = 0;
     int64_t hits = 0, misses = 0, bytes = 0;
 };
@@ -40,6 +41,45 @@ namespace {
 
 size_t expert_code_bytes(const tq_qweight_t& w) { return (size_t)w.rows * w.row_stride_words * 4; }
 size_t expert_scale_bytes(const tq_qweight_t& w) { return (size_t)w.rows * (w.cols / w.group) * 2; }
+
+// One launch copies every missing expert: the threads of the grid walk each segment in turn with
+// 16-byte loads straight from the pinned bank (mapped into the device's address space, read over
+// the CPU-GPU link), four loads in flight per thread.
+constexpr int kMaxSegs = 64;
+struct CopySegs {
+    const uint4* src[kMaxSegs];
+    uint4* dst[kMaxSegs];
+    int64_t n16[kMaxSegs];  // 16-byte pieces
+    int nseg;
+};
+
+__global__ void __launch_bounds__(256) stream_copy_kernel(const CopySegs cs) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int sg = 0; sg < cs.nseg; ++sg) {
+        const uint4* __restrict__ src = cs.src[sg];
+        uint4* __restrict__ dst = cs.dst[sg];
+        const int64_t n = cs.n16[sg];
+        int64_t i = t;
+        for (; i + 3 * stride < n; i += 4 * stride) {
+            const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+            dst[i] = a;
+            dst[i + stride] = b;
+            dst[i + 2 * stride] = c;
+            dst[i + 3 * stride] = d;
+        }
+        for (; i < n; i += stride) dst[i] = src[i];
+    }
+}
+
+bool device_readable(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
 
 // LRU bookkeeping of one step: the slot of every id in slots_out[], and miss[i] = 1 for the
 // first occurrence of each expert that has to be copied.  Hits and misses count distinct
@@ -118,6 +158,10 @@ extern "C" tq_status tq_expert_cache_create(const tq_qweight_t* host_bank, int32
     c->last_use.assign(slots, 0);
     c->expert_slot.assign(host_bank->experts, -1);
     c->seen.assign(host_bank->experts, 0);
+    const size_t cbytes = expert_code_bytes(c->host), sbytes = expert_scale_bytes(c->host);
+    c->kernel_copy = cbytes % 16 == 0 && sbytes % 16 == 0 && aligned(c->host.codes, 16) &&
+                     aligned(c->host.scales, 16) && aligned(dev_codes, 16) && aligned(dev_scales, 16) &&
+                     device_readable(c->host.codes) && device_readable(c->host.scales);
     *out = c;
     return TQ_OK;
 }
@@ -139,6 +183,34 @@ extern "C" tq_status tq_expert_cache_map(tq_expert_cache* c, const int32_t* ids,
     if (s != TQ_OK) return s;
     const size_t cb = expert_code_bytes(c->host), sb = expert_scale_bytes(c->host);
     cudaStream_t st = as_stream(stream);
+    if (c->kernel_copy) {
+        CopySegs segs{};
+        auto flush = [&]() -> tq_status {
+            if (segs.nseg == 0) return TQ_OK;
+            int sms = 0, dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            stream_copy_kernel<<<4 * (sms > 0 ? sms : 152), 256, 0, st>>>(segs);
+            segs.nseg = 0;
+            return launch_status();
+        };
+        for (int i = 0; i < n; ++i) {
+            if (!miss[i]) continue;
+            const int e = ids[i], v = slots[i];
+            if (segs.nseg + 2 > kMaxSegs) {
+                const tq_status fs = flush();
+                if (fs != TQ_OK) return fs;
+            }
+            segs.src[segs.nseg] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(c->host.codes) + (size_t)e * cb);
+            segs.dst[segs.nseg] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(c->dev_codes) + (size_t)v * cb);
+            segs.n16[segs.nseg++] = (int64_t)(cb / 16);
+            segs.src[segs.nseg] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(c->host.scales) + (size_t)e * sb);
+            segs.dst[segs.nseg] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(c->dev_scales) + (size_t)v * sb);
+            segs.n16[segs.nseg++] = (int64_t)(sb / 16);
+            c->bytes += (int64_t)(cb + sb);
+        }
+        return flush();
+    }
     for (int i = 0; i < n; ++i) {
         if (!miss[i]) continue;
         const int e = ids[i], v = slots[i];
