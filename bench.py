@@ -881,7 +881,14 @@ def main():
         def variant(fn):
             return b2b_graph_us(torch, [lambda i=i: fn(logits_all[i:i + 1], x_all[i:i + 1]) for i in range(nv)])
 
-        step_variants = {"headline_two_streams_us": variant(step_on),
+        def step_one_launch_on(logits, x):  # the whole layer as one cooperative launch
+            return tq.moe_decode_layer(qgu, qdn, rotH, rotI, logits.view(-1), x.view(-1), TOPK)
+
+        try:
+            one_launch = variant(step_one_launch_on)
+        except (RuntimeError, tq.TQError) as exc:
+            one_launch = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+        step_variants = {"headline_two_streams_us": variant(step_on), "one_launch_us": one_launch,
                          "one_stream_us": variant(step_serial_on),
                          "swiglu_in_down_us": variant(step_fused_down_on),
                          "rotation_in_gate_up_too_us": variant(step_all_fused_on),

@@ -392,6 +392,33 @@ tq_status tq_kv_attend_noalloc(const void* q, tq_dtype qdt, int32_t Hq, int32_t 
                                void* stream);
 size_t tq_kv_attend_noalloc_max_scratch_bytes(void);
 
+/* ------------------------------------------------------------------ fused decode layer */
+
+/* One token through a Mixture-of-Experts layer in one launch: route (top-k of
+ * the E logits, softmax over the k), rotate x (rot_h), gate||up gather, SwiGLU
+ * and the intermediate rotation (rot_i) of each routed expert's output, down
+ * gather, out = sum_j probs[j] * down_j.  "How it works", "Running a quantized
+ * layer" and the Kimi-K2 router of "Running a 1T-Parameter Model on a Laptop".
+ * One cooperative launch whose phases meet at grid barriers (each wait bounded
+ * by the wait budget: TQ_DEVERR_TIMEOUT in *err on expiry), after a 4-byte
+ * memset of the barrier counter in ws; the arithmetic is that of tq_moe_route,
+ * tq_rotate, tq_gather_qmv, tq_swiglu_rotate, tq_multi_gather_qmv and
+ * tq_moe_combine in sequence, with the same bits.
+ * gate_up: ternary bank, group 16, rows = 2 * down->cols (gate rows first),
+ * cols = H; down: ternary bank, group 16, rows = H, cols = I, the same expert
+ * count E <= 512.  logits: device f32 [E]; x: device [H] of xdt; out: device
+ * [H] of odt (f32 or bf16); k <= 32.  ws: device scratch of
+ * tq_moe_decode_layer_workspace_bytes(gate_up, down, k) bytes, 256-byte
+ * aligned; calls that may run at the same time must not share it.
+ * TQ_ERR_UNSUPPORTED for shapes this launch does not take (then call the
+ * separate entry points): H a multiple of 1024 rotated in blocks of 1024 into
+ * 2 to 8 table-lookup slices, I = 2048 rotated as one block of 2048. */
+size_t tq_moe_decode_layer_workspace_bytes(const tq_qweight_t* gate_up, const tq_qweight_t* down, int32_t k);
+tq_status tq_moe_decode_layer(const tq_qweight_t* gate_up, const tq_qweight_t* down, const tq_rotation_t* rot_h,
+                              const tq_rotation_t* rot_i, const float* logits, const void* x, tq_dtype xdt,
+                              int32_t k, void* out, tq_dtype odt, void* ws, size_t ws_bytes, uint32_t* err,
+                              void* stream);
+
 /* ------------------------------------------------------------------ persisted packed layers (host) */
 
 /* Per-layer tiers and a persisted packed format.

@@ -91,6 +91,9 @@ _SIGS = {
     "tq_kv_attend_noalloc": (_i32, [_c_p, _i32, _i32, _i32, _i32, _i64, _i64, _P(tq_rotation_t), _P(tq_codebook_t),
                                     _P(tq_codebook_t), _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "tq_kv_attend_noalloc_max_scratch_bytes": (_sz, []),
+    "tq_moe_decode_layer_workspace_bytes": (_sz, [_P(tq_qweight_t), _P(tq_qweight_t), _i32]),
+    "tq_moe_decode_layer": (_i32, [_P(tq_qweight_t), _P(tq_qweight_t), _P(tq_rotation_t), _P(tq_rotation_t), _c_p,
+                                   _c_p, _i32, _i32, _c_p, _i32, _c_p, _sz, _c_p, _c_p]),
     "tq_check_error": (_i32, [_c_p, _P(_u32), _c_p]),
     "tq_set_wait_budget": (_i32, [_i64]),
     "tq_rotation_dense": (_i32, [ctypes.c_uint64, _i32, _P(ctypes.c_double)]),
@@ -543,6 +546,24 @@ def kv_attend_noalloc(cache: KVCache, q, ctx: int | None = None):
                                        _ptr(cache.kcodes), _ptr(cache.kscales), _ptr(cache.vcodes),
                                        _ptr(cache.vscales), _ptr(o), _stream()), "tq_kv_attend_noalloc")
     return o
+
+
+def moe_decode_layer(gate_up: QWeight, down: QWeight, rot_h: Rotation, rot_i: Rotation, logits, x, k: int,
+                     out_dtype=None, err=None, ws=None):
+    """One token through the MoE layer in one launch: route, rotate, gate||up, SwiGLU + rotate, down,
+    combine.  logits: f32 [E] (or [1, E]); x: [H] (or [1, H]) f32/bf16/f16.  Returns out [1, H]."""
+    torch = _torch()
+    _contig(logits, "logits")
+    _contig(x, "x")
+    H = gate_up.cols
+    out = torch.empty((1, H), dtype=out_dtype or torch.float32, device=x.device)
+    g, d, rh, ri = gate_up.c(), down.c(), rot_h.c(), rot_i.c()
+    nb = int(load().tq_moe_decode_layer_workspace_bytes(ctypes.byref(g), ctypes.byref(d), k))
+    ws = _workspace(nb, x.device, ws)
+    _check(load().tq_moe_decode_layer(ctypes.byref(g), ctypes.byref(d), ctypes.byref(rh), ctypes.byref(ri),
+                                      _ptr(logits), _ptr(x), _dt(x), k, _ptr(out), _dt(out), _ptr(ws), nb, _ptr(err),
+                                      _stream()), "tq_moe_decode_layer")
+    return out
 
 
 def check_error(err) -> int:

@@ -7,6 +7,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "route.cuh"
 
 using namespace tq;
 
@@ -14,71 +15,17 @@ namespace {
 
 constexpr int kMaxK = 32;
 
-// One warp per token: the row's logits are read once into registers (lane l
-// holds experts l, l + 32, ...), then k rounds of a warp arg-max over the
-// not-yet-taken experts (ties to the lower id; two warp-wide reductions per
-// round), then a softmax over the k chosen logits.  counts (if not NULL)
-// receives each chosen expert's pair count.
+// One warp per token: route_token (the routing body shared with the fused decode layer).
 template <int kPer>  // experts per lane: E <= 32 * kPer
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ ids, float* __restrict__ probs,
                                                          int32_t* __restrict__ counts) {
     pdl_trigger();
     pdl_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
-    const float* row = logits + (int64_t)t * E;
-    float v[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int i = lane + 32 * j;
-        v[j] = i < E ? __ldg(row + i) : -INFINITY;
-    }
-    unsigned taken = 0;  // bit j: expert lane + 32 j already chosen
-    float chosen_v = 0.f;  // lane r keeps the r-th chosen logit
-    // The lane's best untaken expert (ascending ids within the lane: strict > keeps the lower id);
-    // only the lane that wins a round looks again.
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    auto lane_best = [&]() {
-        bv = -INFINITY;
-        bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int i = lane + 32 * j;
-            if (i < E && !(taken >> j & 1u) && (v[j] > bv || bi == 0x7fffffff)) {
-                bv = v[j];
-                bi = i;
-            }
-        }
-    };
-    lane_best();
-    for (int r = 0; r < k; ++r) {
-        // round winner: the largest value (an order-preserving 32-bit key, 0 for a lane with no
-        // candidate), then the lowest id among the lanes holding it -- two warp reductions
-        const uint32_t u0 = __float_as_uint(bv);
-        const uint32_t u = (u0 << 1) == 0u ? 0u : u0;  // -0 and +0 are one value
-        const uint32_t key = bi == 0x7fffffff ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
-        const uint32_t mk = __reduce_max_sync(kFull, key);
-        const uint32_t wi = __reduce_min_sync(kFull, key == mk && bi != 0x7fffffff ? (uint32_t)bi : 0xffffffffu);
-        if ((int)(wi & 31u) == lane) {
-            taken |= 1u << (wi >> 5);
-            lane_best();
-        }
-        if (lane == 0) {
-            ids[(int64_t)t * k + r] = (int32_t)wi;
-            if (counts) atomicAdd(counts + wi, 1);
-        }
-        if (lane == r) chosen_v = __uint_as_float((mk & 0x80000000u) ? (mk ^ 0x80000000u) : ~mk);
-    }
-    // softmax over the k chosen logits; the first is the largest
-    const float mx = __shfl_sync(kFull, chosen_v, 0);
-    const float ex = lane < k ? expf(chosen_v - mx) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(kFull, sum, m);
-    if (lane < k) probs[(int64_t)t * k + lane] = ex / sum;
+    route_token<kPer>(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, probs + (int64_t)t * k, counts);
 }
 
 // offsets[e] = sum of counts below e (one CTA, E <= 1024).

@@ -42,6 +42,7 @@
 #include <algorithm>
 
 #include "qmv_impl.cuh"
+#include "route.cuh"
 
 namespace tq {
 namespace {
@@ -180,11 +181,13 @@ struct LutStream {
     bool bad;           // expert id outside the bank: the stage reads as zeros
 };
 
-// Point the stream at `row` of `item` (reads the item's expert id).
+// Point the stream at `row` of `item` (reads the item's expert id; COH: through L2, for ids
+// written earlier by the same launch).
+template <bool COH>
 TQ_DEVFN void lut_seek(LutStream& st, const QmvParams& p, int item, int row, int64_t wofs, int64_t gofs, int lane) {
     st.item = item;
     st.row = row;
-    const int e = p.mode == kModeDense ? 0 : __ldg(p.ids + item);
+    const int e = p.mode == kModeDense ? 0 : (COH ? __ldcg(p.ids + item) : __ldg(p.ids + item));
     st.bad = e < 0 || e >= p.experts;
     if (st.bad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
     const int64_t ee = st.bad ? 0 : e;
@@ -193,6 +196,7 @@ TQ_DEVFN void lut_seek(LutStream& st, const QmvParams& p, int item, int row, int
 }
 
 // Request the stream's next stage (2 rows) into the ring slot at shared address dst, then advance.
+template <bool COH>
 TQ_DEVFN void lut_issue(LutStream& st, const QmvParams& p, int n_items, int rt_n, uint32_t dst, bool wok, bool gok,
                         int64_t wofs, int64_t gofs, int lane) {
 #pragma unroll
@@ -205,26 +209,24 @@ TQ_DEVFN void lut_issue(LutStream& st, const QmvParams& p, int n_items, int rt_n
     }
     st.row += kLRows;
     if (st.row >= rt_n * kLRows) {
-        if (st.item + 1 < n_items) lut_seek(st, p, st.item + 1, 0, wofs, gofs, lane);
+        if (st.item + 1 < n_items) lut_seek<COH>(st, p, st.item + 1, 0, wofs, gofs, lane);
     } else {
         st.c += kLRows * p.row_stride;
         st.s += kLRows * p.ngroups;
     }
 }
 
-__global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams lp) {
+// The matvec of CTA `cta` of the launch (the table-lookup kernel, or a phase of the fused decode
+// layer).  sm: the 128-byte aligned shared memory of the layout above.  COH: the ids and the
+// input were written earlier by the same launch, so they are read through L2.
+template <bool COH>
+TQ_DEVFN void lut_body(const LutParams& lp, uint8_t* sm, int cta) {
     const QmvParams& p = lp.q;
-    extern __shared__ __align__(16) uint8_t smraw[];
-    const uint32_t raw_addr = smem_u32(smraw);
-    uint8_t* sm = smraw + (((raw_addr + 127u) & ~127u) - raw_addr);
     uint32_t* table = reinterpret_cast<uint32_t*>(sm + kOffTable);
     int16_t* xq = reinterpret_cast<int16_t*>(sm + kOffXq);
     float* xsg = reinterpret_cast<float*>(sm + kOffXs);
-
-    pdl_trigger();  // the slice sum (or the next call) may launch; it waits for this grid
-    pdl_wait();     // ids, x, y and the scratch may belong to the kernel before
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int slice = blockIdx.x / lp.cta_per_slice, cb = blockIdx.x - slice * lp.cta_per_slice;
+    const int slice = cta / lp.cta_per_slice, cb = cta - slice * lp.cta_per_slice;
     const int rt_n = lp.row_tasks, n_items = lp.n_items;
     const int64_t ntasks = (int64_t)n_items * rt_n;
     const int t_begin = (int)(cb * ntasks / lp.cta_per_slice);
@@ -266,15 +268,16 @@ __global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams l
 #pragma unroll
             for (int r = 0; r < kXPer; ++r) {
                 const int f = tid + r * kLThreads, c = col0 + 4 * f;
-                xv4[r] = f < kLSliceCols / 4 && c < p.cols ? __ldg(reinterpret_cast<const float4*>(xv + c))
+                const float4* src = reinterpret_cast<const float4*>(xv + c);
+                xv4[r] = f < kLSliceCols / 4 && c < p.cols ? (COH ? __ldcg(src) : __ldg(src))
                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        if (nmine > 0) lut_seek(st, p, ta / rt_n, (ta % rt_n) * kLRows, wofs, gofs, lane);
+        if (nmine > 0) lut_seek<COH>(st, p, ta / rt_n, (ta % rt_n) * kLRows, wofs, gofs, lane);
         // the first stages go out before the table is (re)built
 #pragma unroll
         for (int j = 0; j < kLDepth - 1; ++j) {
-            if (j < nmine) lut_issue(st, p, n_items, rt_n, ring + j * kLStage, wok, gok, wofs, gofs, lane);
+            if (j < nmine) lut_issue<COH>(st, p, n_items, rt_n, ring + j * kLStage, wok, gok, wofs, gofs, lane);
             cp_commit();
         }
         if (new_vec) {
@@ -340,8 +343,8 @@ __global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams l
         int o_item = ta / rt_n, o_row = (ta % rt_n) * kLRows;
         for (int j = 0; j < nmine; ++j) {
             if (j + kLDepth - 1 < nmine)
-                lut_issue(st, p, n_items, rt_n, ring + ((j + kLDepth - 1) % kLDepth) * kLStage, wok, gok, wofs, gofs,
-                          lane);
+                lut_issue<COH>(st, p, n_items, rt_n, ring + ((j + kLDepth - 1) % kLDepth) * kLStage, wok, gok, wofs,
+                               gofs, lane);
             cp_commit();
             cp_wait<kLDepth - 1>();  // this lane's pieces of stage j have landed
             __syncwarp();            // ... and every lane's
@@ -384,6 +387,15 @@ __global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams l
         cp_wait<0>();
         s0 = s1;
     }
+}
+
+__global__ void __launch_bounds__(kLThreads, 1) qmv_lut_kernel(const LutParams lp) {
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const uint32_t raw_addr = smem_u32(smraw);
+    uint8_t* sm = smraw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    pdl_trigger();  // the slice sum (or the next call) may launch; it waits for this grid
+    pdl_wait();     // ids, x, y and the scratch may belong to the kernel before
+    lut_body<false>(lp, sm, blockIdx.x);
 }
 
 // y[i] = sum over slices of part[s][i], in slice order.
@@ -461,4 +473,279 @@ tq_status qmv_lut_run(const QmvParams& qp, int n_items, void* ws, size_t ws_byte
     return TQ_OK;
 }
 
+
+// ---------------------------------------------------------------- the fused decode layer
+
+namespace {
+
+// One token through a Mixture-of-Experts layer in one cooperative launch: route + input rotation,
+// the gate||up gather, SwiGLU + the intermediate rotation of each routed pair, the down
+// gather, the router-weighted combine.  Phases are separated by grid barriers (a counter the
+// host zeroes before the launch; each wait bounded by the wait budget, after which the CTA
+// raises TQ_DEVERR_TIMEOUT and stops).  Every phase does what the separate kernels do, in the
+// same order of operations, so the result has their bits.
+struct DecodeParams {
+    LutParams gu, dn;  // the two matvec phases
+    const float* logits;
+    int E, k;
+    const void* x;
+    int xdt;
+    const int8_t* sig_h;
+    int H, block_h, span_h;
+    float scale_h;
+    const int8_t* sig_i;
+    int I, block_i;
+    float scale_i;
+    float* x_rot;   // [H]
+    int32_t* ids;   // [k]
+    float* probs;   // [k]
+    float* h_rot;   // [k][I]
+    float* y_dn;    // [k][H]
+    void* out;      // [H]
+    int odt;
+    unsigned* bar;  // grid barrier counter, zero at launch
+    uint32_t* err;
+    long long wait_cycles;
+};
+
+// All CTAs of the launch meet; false (and TQ_DEVERR_TIMEOUT) if the others did not arrive in time.
+TQ_DEVFN bool grid_meet(const DecodeParams& dp, unsigned target, int* flag) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(dp.bar, 1u);
+        const long long t0 = clock64();
+        int ok = 1;
+        while (*reinterpret_cast<volatile unsigned*>(dp.bar) < target) {
+            if (clock64() - t0 > dp.wait_cycles) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        if (!ok && dp.err) atomicOr(dp.err, TQ_DEVERR_TIMEOUT);
+        *flag = ok;
+    }
+    __syncthreads();
+    return *flag != 0;
+}
+
+template <int EH, int EI>
+__global__ void __launch_bounds__(kLThreads, 1) moe_decode_kernel(const DecodeParams dp) {
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const uint32_t raw_addr = smem_u32(smraw);
+    uint8_t* sm = smraw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    float* fw = reinterpret_cast<float*>(sm);  // transform scratch of the rotation phases
+    __shared__ int flag;
+    const int cta = blockIdx.x, tid = threadIdx.x, G = gridDim.x;
+    pdl_trigger();
+    pdl_wait();
+    // phase 1: the input rotation (one CTA per span of whole Hadamard blocks) and the router
+    const int nrot = dp.H / dp.span_h;
+    if (cta < nrot) {
+        const int base = cta * dp.span_h + tid * EH;
+        float v[EH];
+#pragma unroll
+        for (int i = 0; i < EH; ++i) v[i] = load_as_float(dp.x, base + i, dp.xdt) * (float)dp.sig_h[base + i];
+        fwht_cta<EH>(v, fw, dp.block_h);
+#pragma unroll
+        for (int i = 0; i < EH; ++i) dp.x_rot[base + i] = v[i] * dp.scale_h;
+    } else if (cta == nrot && tid < 32) {
+        route_token<16>(dp.logits, dp.E, dp.k, dp.ids, dp.probs, nullptr);
+    }
+    if (!grid_meet(dp, 1u * G, &flag)) return;
+    // phase 2: gate||up of the k routed experts (column slices: partial sums)
+    if (cta < dp.gu.cta_per_slice * dp.gu.nslices) lut_body<true>(dp.gu, sm, cta);
+    if (!grid_meet(dp, 2u * G, &flag)) return;
+    // phase 3: per pair, the slices' sum (in slice order), silu(gate) * up, the rotation
+    if (cta < dp.k) {
+        const int64_t n = (int64_t)dp.k * 2 * dp.I;
+        const float* a = dp.gu.part + (int64_t)cta * 2 * dp.I;
+        const int base = tid * EI;
+        float v[EI];
+#pragma unroll
+        for (int i = 0; i < EI; ++i) {
+            float g = 0.f, u = 0.f;
+            for (int sl = 0; sl < dp.gu.nslices; ++sl) {
+                g += __ldcg(a + sl * n + base + i);
+                u += __ldcg(a + sl * n + dp.I + base + i);
+            }
+            v[i] = g / (1.0f + expf(-g)) * u * (float)dp.sig_i[base + i];
+        }
+        fwht_cta<EI>(v, fw, dp.block_i);
+#pragma unroll
+        for (int i = 0; i < EI; ++i) dp.h_rot[(int64_t)cta * dp.I + base + i] = v[i] * dp.scale_i;
+    }
+    if (!grid_meet(dp, 3u * G, &flag)) return;
+    // phase 4: down projection of each pair (one column slice: y directly)
+    if (cta < dp.dn.cta_per_slice * dp.dn.nslices) lut_body<true>(dp.dn, sm, cta);
+    if (!grid_meet(dp, 4u * G, &flag)) return;
+    // phase 5: out = sum_j probs[j] y_j
+    for (int c = cta * kLThreads + tid; c < dp.H; c += G * kLThreads) {
+        float acc = 0.f;
+        for (int j = 0; j < dp.k; ++j) acc = fmaf(__ldcg(dp.probs + j), __ldcg(dp.y_dn + (int64_t)j * dp.H + c), acc);
+        store_from_float(dp.out, c, dp.odt, acc);
+    }
+}
+
+// The span of whole Hadamard blocks one rotation CTA takes (as the rotation kernel chooses it).
+int decode_span(int dim, int block) {
+    int span = block;
+    while (span * 2 <= 2048 && dim % (span * 2) == 0) span *= 2;
+    return span;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct DecodeLayout {
+    size_t bar, ids, probs, xrot, part, hrot, ydn, total;
+};
+
+DecodeLayout decode_layout(int H, int I, int k) {
+    DecodeLayout L{};
+    size_t o = 0;
+    L.bar = o;
+    o += 256;
+    L.ids = o;
+    o += align256((size_t)k * 4);
+    L.probs = o;
+    o += align256((size_t)k * 4);
+    L.xrot = o;
+    o += align256((size_t)H * 4);
+    L.part = o;
+    o += align256((size_t)lut_nslices(H) * k * 2 * I * 4);
+    L.hrot = o;
+    o += align256((size_t)k * I * 4);
+    L.ydn = o;
+    o += align256((size_t)k * H * 4);
+    L.total = o;
+    return L;
+}
+
+bool decode_ok(const tq_qweight_t* gu, const tq_qweight_t* dn, const tq_rotation_t* rh, const tq_rotation_t* ri,
+               int k) {
+    if (!gu || !dn || !rh || !ri || !rh->signs || !ri->signs) return false;
+    const int H = gu->cols, I = dn->cols;
+    if (gu->cb.levels != 3 || dn->cb.levels != 3 || gu->group != 16 || dn->group != 16) return false;
+    if (gu->rows != 2 * I || dn->rows != H || gu->experts != dn->experts || gu->experts > 512) return false;
+    if (k < 1 || k > 32 || k > gu->experts || rh->dim != H || ri->dim != I) return false;
+    if (lut_nslices(I) != 1 || lut_nslices(H) > 8) return false;
+    const int sh = decode_span(H, rh->block), si = decode_span(I, ri->block);
+    return sh == 2 * kLThreads && si == 4 * kLThreads && H % sh == 0 && I % si == 0 && I == si &&
+           H / sh < 152;
+}
+
+}  // namespace
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" size_t tq_moe_decode_layer_workspace_bytes(const tq_qweight_t* gate_up, const tq_qweight_t* down,
+                                                      int32_t k) {
+    if (!gate_up || !down || k < 1) return 0;
+    return decode_layout(gate_up->cols, down->cols, k).total;
+}
+
+extern "C" tq_status tq_moe_decode_layer(const tq_qweight_t* gate_up, const tq_qweight_t* down,
+                                         const tq_rotation_t* rot_h, const tq_rotation_t* rot_i,
+                                         const float* logits, const void* x, tq_dtype xdt, int32_t k, void* out,
+                                         tq_dtype odt, void* ws, size_t ws_bytes, uint32_t* err, void* stream) {
+    if (!gate_up || !down || !logits || !x || !out || !ws) return TQ_ERR_INVALID;
+    if (!(xdt == TQ_F32 || xdt == TQ_BF16 || xdt == TQ_F16) || !(odt == TQ_F32 || odt == TQ_BF16))
+        return TQ_ERR_INVALID;
+    if (!gate_up->codes || !gate_up->scales || !down->codes || !down->scales || !gate_up->cb.centroids ||
+        !down->cb.centroids)
+        return TQ_ERR_INVALID;
+    if (!decode_ok(gate_up, down, rot_h, rot_i, k)) return TQ_ERR_UNSUPPORTED;
+    const int H = gate_up->cols, I = down->cols;
+    const DecodeLayout L = decode_layout(H, I, k);
+    if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return TQ_ERR_INVALID;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    DecodeParams dp{};
+    dp.logits = logits;
+    dp.E = gate_up->experts;
+    dp.k = k;
+    dp.x = x;
+    dp.xdt = xdt;
+    dp.sig_h = rot_h->signs;
+    dp.H = H;
+    dp.block_h = rot_h->block;
+    dp.span_h = decode_span(H, rot_h->block);
+    dp.scale_h = (float)(1.0 / sqrt((double)rot_h->block));
+    dp.sig_i = rot_i->signs;
+    dp.I = I;
+    dp.block_i = rot_i->block;
+    dp.scale_i = (float)(1.0 / sqrt((double)rot_i->block));
+    dp.bar = reinterpret_cast<unsigned*>(b + L.bar);
+    dp.ids = reinterpret_cast<int32_t*>(b + L.ids);
+    dp.probs = reinterpret_cast<float*>(b + L.probs);
+    dp.x_rot = reinterpret_cast<float*>(b + L.xrot);
+    dp.h_rot = reinterpret_cast<float*>(b + L.hrot);
+    dp.y_dn = reinterpret_cast<float*>(b + L.ydn);
+    dp.out = out;
+    dp.odt = odt;
+    dp.err = err;
+    dp.wait_cycles = wait_budget();
+    // the two matvec phases, as the table-lookup kernel would be launched for them
+    auto qparams = [&](const tq_qweight_t* w, const float* xin, int mode, void* y) {
+        QmvParams q{};
+        q.codes = w->codes;
+        q.scales = w->scales;
+        q.row_stride = w->row_stride_words;
+        q.expert_stride_w = w->experts > 1 ? w->expert_stride_words : 0;
+        q.expert_stride_s = w->experts > 1 ? w->expert_stride_scales : 0;
+        q.rows = w->rows;
+        q.cols = w->cols;
+        q.ngroups = w->cols / w->group;
+        q.experts = w->experts;
+        q.centroids = w->cb.centroids;
+        q.levels = 3;
+        q.x = xin;
+        q.T = 1;
+        q.mode = mode;
+        q.ids = dp.ids;
+        q.k = mode == kModeGather ? k : 1;
+        q.y = y;
+        q.ydt = TQ_F32;
+        q.err = err;
+        q.wait_cycles = dp.wait_cycles;
+        return q;
+    };
+    auto lparams = [&](const QmvParams& q, float* part) {
+        LutParams lp{};
+        lp.q = q;
+        lp.nslices = lut_nslices(q.cols);
+        lp.row_tasks = (q.rows + kLRows - 1) / kLRows;
+        lp.n_items = k;
+        const int64_t ntasks = (int64_t)k * lp.row_tasks;
+        lp.cta_per_slice = (int)std::max<int64_t>(1, std::min<int64_t>(sms / lp.nslices, (ntasks + 1) / 2));
+        lp.part = part;
+        return lp;
+    };
+    dp.gu = lparams(qparams(gate_up, dp.x_rot, kModeGather, nullptr), reinterpret_cast<float*>(b + L.part));
+    dp.dn = lparams(qparams(down, dp.h_rot, kModeMulti, dp.y_dn), nullptr);
+    if (!qmv_lut_ok(dp.gu.q, 16) || !qmv_lut_ok(dp.dn.q, 16)) return TQ_ERR_UNSUPPORTED;
+    if (dp.gu.nslices < 2 || dp.dn.nslices != 1) return TQ_ERR_UNSUPPORTED;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(dp.bar, 0, sizeof(unsigned), st) != cudaSuccess) return TQ_ERR_CUDA;
+    if (ensure_smem((const void*)moe_decode_kernel<2, 4>, kLSmem) != cudaSuccess) return TQ_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(kLThreads);
+    cfg.dynamicSmemBytes = kLSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_decode_kernel<2, 4>, dp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+namespace tq {
 }  // namespace tq
