@@ -33,6 +33,8 @@ def nvcc() -> str:
 
 # qmv_inst.cu is compiled once per (levels, group) pair so the templates build in parallel.
 QMV_VARIANTS = [(lv, g) for lv in (3, 4, 8, 16) for g in (16, 32, 64, 128)]
+# qmv_rows.cu: its entry points, then the kernel instances of each bit-packed book.
+ROWS_VARIANTS = (0, 4, 8, 16)
 
 
 def sources() -> list[tuple[str, str, list[str]]]:
@@ -45,6 +47,9 @@ def sources() -> list[tuple[str, str, list[str]]]:
         if f == "qmv_inst.cu":
             for lv, g in QMV_VARIANTS:
                 out.append((src, f"qmv_l{lv}_g{g}.o", [f"-DTQ_LEVELS={lv}", f"-DTQ_GROUP={g}"]))
+        elif f == "qmv_rows.cu":  # the entry points (0), then one unit per bit-packed book
+            for lv in ROWS_VARIANTS:
+                out.append((src, f"qmv_rows_l{lv}.o", [f"-DTQ_ROWS_LEVELS={lv}"]))
         else:
             out.append((src, f[:-3] + ".o", []))
     return out

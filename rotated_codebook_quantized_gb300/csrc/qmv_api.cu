@@ -103,9 +103,10 @@ extern "C" tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T
     QmvParams p = make_params(w, x_rot, y, ydt, nullptr);
     p.mode = kModeDense;
     p.T = T;
-    // Bit-packed books at small T take the staged kernel, one vector per item (later vectors
-    // re-read the weights, mostly from L2).  From T = 16 on, the batched kernel below, which
-    // decodes each weight once for up to 4 vectors, is faster (295 vs 268 us at 11008x4096).
+    // Bit-packed books up to T = 8 take the row-per-lane kernel, which decodes each weight word
+    // once for up to four vectors (a second group of four re-reads the weights, mostly from L2;
+    // 11008 x 4096 3-bit: 17.4 us at T = 1, 27.1 at 4, 45.8 at 8, 84.4 at 16); beyond, the
+    // batched kernel below.
     if (T <= 8 && qmv_rows_ok(p, w->group)) {
         const tq_status rs = qmv_rows_run(p, w->group, T, nullptr, 0, as_stream(stream));
         if (rs != TQ_ERR_UNSUPPORTED) return rs;
@@ -183,7 +184,7 @@ struct GroupLists {
 __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                            GroupLists L, int32_t* __restrict__ cnt, void* y,
                                                            int rows, int ydt, uint32_t* err) {
-    __shared__ int part[3][1024];
+    __shared__ int wsum[3][32];
     __shared__ int any_bad;
     int32_t* fill = cnt + E;
     int32_t* first = fill + E;  // [3][E]
@@ -201,32 +202,43 @@ __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __rest
     // one-slot c%4 == 1; exclusive prefixes over the experts (a contiguous range per thread)
     auto nrec = [](int c, int i) { return i == 0 ? c / 4 + (c % 4 == 3) : (i == 1 ? (c % 4 == 2) : (c % 4 == 1)); };
     const int per = (E + nt - 1) / nt, e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    const int lane = tid & 31, wid = tid >> 5, nwarp = nt >> 5;
+    int loc[3], inc[3];
     for (int i = 0; i < 3; ++i) {
         int local = 0;
         for (int e = e0; e < e1; ++e) local += nrec(cnt[e], i);
-        part[i][tid] = local;
+        loc[i] = inc[i] = local;
+        for (int d = 1; d < 32; d <<= 1) {  // inclusive scan within the warp
+            const int v = __shfl_up_sync(0xffffffffu, inc[i], d);
+            if (lane >= d) inc[i] += v;
+        }
+        if (lane == 31) wsum[i][wid] = inc[i];
+    }
+    __syncthreads();
+    if (wid == 0) {  // inclusive scan of the warps' totals
+        for (int i = 0; i < 3; ++i) {
+            int v = lane < nwarp ? wsum[i][lane] : 0;
+            for (int d = 1; d < 32; d <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += u;
+            }
+            if (lane < nwarp) wsum[i][lane] = v;
+        }
     }
     __syncthreads();
     if (tid < 3) {
-        int acc = 0;
-        for (int t = 0; t < nt; ++t) {
-            const int v = part[tid][t];
-            part[tid][t] = acc;
-            acc += v;
-        }
-        L.list[tid][0] = acc;
+        L.list[tid][0] = wsum[tid][nwarp - 1];
         L.list[tid][1] = 0;
     }
-    __syncthreads();
     for (int i = 0; i < 3; ++i) {
-        int run = part[i][tid];
+        int run = inc[i] - loc[i] + (wid > 0 ? wsum[i][wid - 1] : 0);  // records of the experts before e0
         for (int e = e0; e < e1; ++e) {
             first[i * E + e] = run;
             run += nrec(cnt[e], i);
         }
     }
-    for (int i = 0; i < 3; ++i) {
-        const int nv = i == 0 ? 4 : (i == 1 ? 2 : 1), nr = L.list[i][0];
+    for (int i = 0; i < 3; ++i) {  // the records' slots empty (-1) until their pairs are placed
+        const int nv = i == 0 ? 4 : (i == 1 ? 2 : 1), nr = wsum[i][nwarp - 1];
         for (int j = tid; j < nr * nv; j += nt) L.list[i][2 + (j / nv) * (1 + nv) + 1 + j % nv] = -1;
     }
     __syncthreads();
@@ -258,9 +270,9 @@ __global__ void __launch_bounds__(1024) group_pairs_kernel(const int32_t* __rest
     }
 }
 
-tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaStream_t st) {
+// Builds the record lists in ws (groups_workspace bytes) on the stream.
+tq_status group_pairs(const QmvParams& p, const tq_qweight_t* w, int P, void* ws, GroupLists& L, cudaStream_t st) {
     int32_t* base = static_cast<int32_t*>(ws);
-    GroupLists L;
     int64_t off = 0;
     for (int i = 0; i < 3; ++i) {
         L.list[i] = base + off;
@@ -268,7 +280,39 @@ tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaSt
     }
     int32_t* cnt = base + off;
     group_pairs_kernel<<<1, 1024, 0, st>>>(p.ids, P, w->experts, L, cnt, p.y, p.rows, p.ydt, p.err);
-    tq_status s = launch_status();
+    return launch_status();
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// Scratch of the row-per-lane kernel over grouped pairs: the lists, then the chunks' partial sums.
+size_t rows_groups_workspace(const tq_qweight_t* w, int64_t P) {
+    const size_t g = groups_workspace(w, P);
+    return g ? round256(g) + items_workspace(w, P) : 0;
+}
+
+// Gather (p.mode kModeGather, P = T * k pairs) or multi-gather of bit-packed books through the
+// row-per-lane kernel with the pairs grouped by expert: the lists are built first, then each
+// expert's words are decoded once for up to four of its pairs.
+tq_status run_groups_rows(const QmvParams& p, const tq_qweight_t* w, int P, void* ws, size_t ws_bytes,
+                          cudaStream_t st) {
+    GroupLists L;
+    tq_status s = group_pairs(p, w, P, ws, L, st);
+    if (s != TQ_OK) return s;
+    const size_t off = round256(groups_workspace(w, P));
+    const int32_t* lists[3] = {L.list[0], L.list[1], L.list[2]};
+    return qmv_rows_run_groups(p, w->group, lists, P, static_cast<char*>(ws) + off, ws_bytes - off, st);
+}
+
+// Whether the grouped row-per-lane path takes these pairs with this scratch.
+bool groups_rows_apply(const QmvParams& p, const tq_qweight_t* w, int64_t P, const void* ws, size_t ws_bytes) {
+    const size_t need = rows_groups_workspace(w, P);
+    return need > 0 && qmv_rows_ok(p, w->group) && ws && aligned(ws, 16) && ws_bytes >= need;
+}
+
+tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaStream_t st) {
+    GroupLists L;
+    tq_status s = group_pairs(p, w, P, ws, L, st);
     if (s != TQ_OK) return s;
     p.mode = kModeGroups;
     for (int i = 0; i < 3; ++i) {  // each launch has room for the list's most records; the rest return at once
@@ -282,11 +326,14 @@ tq_status run_groups(QmvParams p, const tq_qweight_t* w, int P, void* ws, cudaSt
 }  // namespace
 
 extern "C" size_t tq_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t T, int32_t k) {
-    return T > 0 && k > 0 ? items_workspace(w, (int64_t)T * k) : 0;
+    if (T <= 0 || k <= 0) return 0;
+    const int64_t P = (int64_t)T * k;
+    // more than one token: room to group the pairs by expert (bit-packed books)
+    return std::max(items_workspace(w, P), T > 1 ? rows_groups_workspace(w, P) : (size_t)0);
 }
 
 extern "C" size_t tq_multi_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t P) {
-    return std::max(items_workspace(w, P), groups_workspace(w, P));
+    return std::max(std::max(items_workspace(w, P), groups_workspace(w, P)), rows_groups_workspace(w, P));
 }
 
 extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t T, int32_t k,
@@ -302,6 +349,8 @@ extern "C" tq_status tq_gather_qmv(const tq_qweight_t* w, const float* x_rot, co
     p.mode = kModeGather;
     p.ids = ids;
     p.k = k;
+    if (T > 1 && groups_rows_apply(p, w, (int64_t)T * k, ws, ws_bytes))
+        return run_groups_rows(p, w, T * k, ws, ws_bytes, as_stream(stream));
     return run_items(p, w->group, T * k, ws, ws_bytes, as_stream(stream));
 }
 
@@ -318,6 +367,7 @@ extern "C" tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_r
     p.mode = kModeMulti;
     p.ids = ids;
     p.k = 1;
+    if (groups_rows_apply(p, w, P, ws, ws_bytes)) return run_groups_rows(p, w, P, ws, ws_bytes, as_stream(stream));
     const size_t gneed = groups_workspace(w, P);
     if (!qmv_rows_ok(p, w->group) && gneed > 0 && ws && ws_bytes >= gneed && aligned(ws, 16))
         return run_groups(p, w, P, ws, as_stream(stream));

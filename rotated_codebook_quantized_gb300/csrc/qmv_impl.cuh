@@ -333,12 +333,18 @@ size_t qmv_lut_workspace_bytes(int cols, int64_t n_items, int rows);
 tq_status qmv_lut_run(const QmvParams& p, int n_items, void* ws, size_t ws_bytes, cudaStream_t st);
 bool qmv_bits_ok(const QmvParams& p, int group);
 tq_status qmv_bits_run(const QmvParams& p, int group, int n_items, cudaStream_t st);
-// Bit-packed books, one matrix row per lane (qmv_rows.cu): every mode but kModeGroups.  Rows
+// Bit-packed books, one matrix row per lane (qmv_rows.cu): every mode but kModeGroups (dense
+// vectors go four, two or one to a task; gather and multi items one pair to a task).  Rows
 // longer than one column chunk need qmv_rows_workspace_bytes of scratch for the chunks'
 // partial sums; without it an f32 output is zeroed and the chunks add into it.
 bool qmv_rows_ok(const QmvParams& p, int group);
 size_t qmv_rows_workspace_bytes(int levels, int group, int cols, int64_t n_items, int rows);
 tq_status qmv_rows_run(const QmvParams& p, int group, int n_items, void* ws, size_t ws_bytes, cudaStream_t st);
+// The same kernel over pairs grouped by expert: lists[i] holds the grouping's records of 4, 2
+// and 1 pairs (count, pad, then expert and pair indices per record), written on the device;
+// each expert's words are decoded once per record.  Scratch as for P items.
+tq_status qmv_rows_run_groups(const QmvParams& p, int group, const int32_t* const lists[3], int P, void* ws,
+                              size_t ws_bytes, cudaStream_t st);
 
 // One entry point per (levels, group), each compiled in its own translation unit.
 #define TQ_QMV_DECL(L, G) tq_status qmv_run_l##L##_g##G(QmvParams p, int nv, int n_items, cudaStream_t st);

@@ -148,6 +148,55 @@ def test_multi_gather_qmv_grouped_record_sizes(lib):
     np.testing.assert_allclose(y, ypp, rtol=1e-5, atol=1e-6 * np.abs(y).max())
 
 
+@pytest.mark.parametrize("levels,group,K,rows", [(8, 128, 1280, 200), (4, 16, 512, 37), (16, 64, 768, 70)])
+def test_qmv_bitpacked_ragged_batches(lib, levels, group, K, rows):
+    """tq_qmv at T = 1 .. 16 (vectors taken four, two and one to a task): every batch against the
+    oracle, and each row equal to the one-vector call up to the order of the column chunks' sums."""
+    qw, Wh = _bank(lib, levels, 1, rows, K, group, seed=90 + levels)
+    W = Wh(0)
+    x = wl.rng(90, levels).normal(size=(16, K)).astype(np.float32)
+    singles = np.stack([lib.qmv(qw, _dev(x[t:t + 1]), tensor_cores=False).cpu().numpy()[0] for t in range(16)])
+    assert rel_l2(singles, o.qmv(W, x)) < BITS_TOL
+    for T in (2, 3, 5, 6, 7, 9, 13, 16):
+        y = lib.qmv(qw, _dev(x[:T]), tensor_cores=False).cpu().numpy()
+        assert rel_l2(y, o.qmv(W, x[:T])) < BITS_TOL, T
+        np.testing.assert_allclose(y, singles[:T], rtol=1e-5, atol=1e-6 * np.abs(singles).max())
+
+
+def test_multi_gather_qmv_grouped_bf16_and_bad_ids(lib):
+    """Grouped pairs with a bf16 output (one column chunk: direct stores) and with an f32 output
+    over several chunks (partial sums in scratch): bad ids give zero rows and BAD_ID, the rest
+    match the oracle (bf16: to its rounding)."""
+    E = 7
+    for K, group in ((320, 64), (2560, 64)):
+        qw, Wh = _bank(lib, 8, E, 100, K, group, seed=91 + K)
+        ids = np.array([2, 2, 6, 2, 2, 2, 9, 0, 6, 2, -1, 3, 3, 3], dtype=np.int32)
+        x = wl.rng(91, K).normal(size=(len(ids), K)).astype(np.float32)
+        good = (ids >= 0) & (ids < E)
+        ref = np.zeros((len(ids), 100))
+        ref[good] = o.multi_gather_qmv(Wh, ids[good], x[good])
+        for dt, tol in ((torch.float32, BITS_TOL), (torch.bfloat16, 8e-3)):
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            y = lib.multi_gather_qmv(qw, _dev(x), _dev(ids), out_dtype=dt, err=err).float().cpu().numpy()
+            assert lib.check_error(err) == lib.TQ_DEVERR_BAD_ID
+            assert np.all(y[~good] == 0)
+            assert rel_l2(y[good], ref[good]) < tol
+
+
+def test_gather_qmv_bitpacked_grouped_tokens(lib):
+    """Eight tokens, top-4 of 24 experts under a skewed router (shared input per token, experts
+    repeated across tokens, grouped by expert): against the oracle and the one-token calls."""
+    E, K, rows, T, k = 24, 1536, 160, 8, 4
+    qw, Wh = _bank(lib, 8, E, rows, K, 64, seed=92)
+    oids, _ = o.route(wl.router_logits(92, T, E, zipf=1.3), k)
+    ids = oids.astype(np.int32)
+    x = wl.rng(92, 8).normal(size=(T, K)).astype(np.float32)
+    y = lib.gather_qmv(qw, _dev(x), _dev(ids)).cpu().numpy()
+    assert rel_l2(y, o.gather_qmv(Wh, ids, x)) < BITS_TOL
+    one = np.stack([lib.gather_qmv(qw, _dev(x[t:t + 1]), _dev(ids[t:t + 1])).cpu().numpy()[0] for t in range(T)])
+    np.testing.assert_allclose(y, one, rtol=1e-5, atol=1e-6 * np.abs(one).max())
+
+
 def test_multi_gather_qmv_ternary_repeats_and_bad_id(lib):
     """Ternary book, per-pair inputs with repeated experts and a bad id (integer input per group: 2.5e-4)."""
     E, rows, K, group = 10, 96, 2048, 16
