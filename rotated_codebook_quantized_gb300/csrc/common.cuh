@@ -184,11 +184,12 @@ TQ_DEVFN void fwht_cta(float (&v)[E], float* s, int block) {  // s: fwht_pad_flo
     h = E;
     for (; h < block && h < 32 * E; h <<= 1) {
         const int m = h / E;
-        const bool upper = lane & m;
+        // the upper lane of a pair keeps o - v, the lower v + o: one fma with a sign of +-1 (exact)
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-            float o = __shfl_xor_sync(kFull, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
+            const float o = __shfl_xor_sync(kFull, v[i], m);
+            v[i] = fmaf(sgn, v[i], o);
         }
     }
     if (h < block) {
@@ -199,11 +200,11 @@ TQ_DEVFN void fwht_cta(float (&v)[E], float* s, int block) {  // s: fwht_pad_flo
 #pragma unroll
             for (int i = 0; i < E; ++i) s[(base + i) + ((base + i) >> 5)] = v[i];
             __syncthreads();
+            const float sgn = (base & h) ? -1.0f : 1.0f;  // h >= 32 E: the same side for all of the thread's E
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                const int idx = base + i, j = idx ^ h;
-                float o = s[j + (j >> 5)];
-                v[i] = (idx & h) ? (o - v[i]) : (v[i] + o);
+                const int j = (base + i) ^ h;
+                v[i] = fmaf(sgn, v[i], s[j + (j >> 5)]);
             }
             __syncthreads();
         }

@@ -49,21 +49,59 @@ TQ_DEVFN uint32_t pack_word(const uint8_t* codes, int n, int j, int levels, int 
     return w;
 }
 
-template <int E>
+// Number of thresholds strictly below u, the book's thresholds in registers (unrolled).
+template <int NT>
+TQ_DEVFN uint32_t snap_reg(float u, const float (&t)[NT]) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) c += (t[i] < u) ? 1u : 0u;
+    return c;
+}
+
+// Word j of a packed row of a book of LEVELS codes from the codes in shared memory (0 beyond n).
+template <int LEVELS>
+TQ_DEVFN uint32_t pack_word_l(const uint8_t* codes, int n, int j) {
+    constexpr int kCW = LEVELS == 3 ? 20 : (LEVELS == 8 ? 10 : (LEVELS == 4 ? 16 : 8));
+    constexpr int kBits = LEVELS == 4 ? 2 : (LEVELS == 8 ? 3 : 4);
+    uint32_t w = 0;
+    const int k0 = j * kCW;
+    if (k0 + kCW <= n) {
+#pragma unroll
+        for (int i = kCW - 1; i >= 0; --i) {
+            const uint32_t c = codes[k0 + i];
+            if constexpr (LEVELS == 3) w = w * 3u + c;
+            else w |= c << (kBits * i);
+        }
+    } else {
+#pragma unroll
+        for (int i = kCW - 1; i >= 0; --i) {
+            const uint32_t c = k0 + i < n ? codes[k0 + i] : 0u;
+            if constexpr (LEVELS == 3) w = w * 3u + c;
+            else w |= c << (kBits * i);
+        }
+    }
+    return w;
+}
+
+// One CTA per row of cols = threads * E values: rotate (signs, FWHT blocks, 1/sqrt(block)), group
+// RMS, snap each u = v / RMS (through one reciprocal per group) to the book of LEVELS codes,
+// pack.  The thresholds sit in registers and every loop over codes is unrolled.
+template <int E, int LEVELS>
 __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restrict__ W, int wdt, int cols, int group,
                                                              int block, float rscale, const int8_t* __restrict__ signs,
-                                                             const float* __restrict__ thresholds, int levels,
+                                                             const float* __restrict__ thresholds,
                                                              uint32_t* __restrict__ codes, uint16_t* __restrict__ scales,
                                                              int64_t row_stride) {
+    constexpr int NT = LEVELS - 1;
     extern __shared__ float smem[];
     float* fw = smem;                                           // fwht_pad_floats(cols) (FWHT exchange)
-    float* thr = smem + fwht_pad_floats(cols);                  // levels-1 thresholds
-    uint8_t* cd = reinterpret_cast<uint8_t*>(thr + 256);        // cols codes
+    uint8_t* cd = reinterpret_cast<uint8_t*>(smem + fwht_pad_floats(cols) + 256);  // cols codes
     const int64_t row = blockIdx.x;
     const int base = threadIdx.x * E;
     const int lane = threadIdx.x & 31;
-    const int nthr = levels - 1;
-    for (int i = threadIdx.x; i < nthr; i += blockDim.x) thr[i] = thresholds[i];
+    float thr[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) thr[i] = __ldg(thresholds + i);
 
     float v[E];
     const int64_t off = row * cols + base;
@@ -94,6 +132,9 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
 
     const float inv_g = 1.0f / (float)group;
     const int ngroups = cols / group;
+    uint32_t cpk[(E + 3) / 4];  // the thread's codes, four bytes to a word
+#pragma unroll
+    for (int q = 0; q < (E + 3) / 4; ++q) cpk[q] = 0u;
     if (E >= 16 && group <= 16) {  // a thread holds whole groups (E = 16, group 16): fixed indices
 #pragma unroll
         for (int g0 = 0; g0 < E; g0 += 16) {
@@ -102,11 +143,9 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
             for (int i = g0; i < g0 + 16; ++i) ss += v[i] * v[i];
             const float s = sqrtf(ss * inv_g);
             scales[row * ngroups + (base + g0) / 16] = __half_as_ushort(__float2half_rn(s));
+            const float r = s > 0.f ? 1.0f / s : 0.f;
 #pragma unroll
-            for (int i = g0; i < g0 + 16; ++i) {
-                const float u = s > 0.f ? __fdiv_rn(v[i], s) : 0.f;
-                cd[base + i] = (uint8_t)snap_code(u, thr, nthr);
-            }
+            for (int i = g0; i < g0 + 16; ++i) cpk[i >> 2] |= snap_reg(v[i] * r, thr) << (8 * (i & 3));
         }
     } else {
         const int lpg = group / E;  // lanes per group, 2..32
@@ -116,17 +155,20 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
         for (int m = 1; m < lpg; m <<= 1) ss += __shfl_xor_sync(kFull, ss, m);
         const float s = sqrtf(ss * inv_g);
         if ((lane & (lpg - 1)) == 0) scales[row * ngroups + base / group] = __half_as_ushort(__float2half_rn(s));
+        const float r = s > 0.f ? 1.0f / s : 0.f;
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const float u = s > 0.f ? __fdiv_rn(v[i], s) : 0.f;
-            cd[base + i] = (uint8_t)snap_code(u, thr, nthr);
-        }
+        for (int i = 0; i < E; ++i) cpk[i >> 2] |= snap_reg(v[i] * r, thr) << (8 * (i & 3));
+    }
+    if constexpr (E >= 4) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) reinterpret_cast<uint32_t*>(cd + base)[q] = cpk[q];
+    } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) cd[base + i] = (uint8_t)(cpk[0] >> (8 * i));
     }
     __syncthreads();
-    const int cw = levels == 3 ? 20 : (levels == 8 ? 10 : 32 / (31 - __clz(levels)));
-    const int bits = 31 - __clz(levels);
     for (int64_t j = threadIdx.x; j < row_stride; j += blockDim.x)
-        codes[row * row_stride + j] = pack_word(cd, cols, (int)j, levels, cw, bits);
+        codes[row * row_stride + j] = pack_word_l<LEVELS>(cd, cols, (int)j);
 }
 
 // One warp encodes one D = 128 vector (4 values per lane), used for K and V.
@@ -443,6 +485,29 @@ __global__ void __launch_bounds__(256) quantize_diag_kernel(const void* __restri
         codes[row * row_stride + j] = pack_word(cd, cols, (int)j, levels, cw, bits);
 }
 
+template <int E, int LEVELS>
+tq_status quantize_rows_launch(const void* W, tq_dtype wdt, int64_t rows, int32_t cols, int32_t group,
+                               const tq_rotation_t* rot, const tq_codebook_t* cb, uint32_t* codes, uint16_t* scales,
+                               int64_t row_stride_words, size_t smem, float rscale, cudaStream_t st) {
+    if (ensure_smem((const void*)quantize_rows_kernel<E, LEVELS>, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    quantize_rows_kernel<E, LEVELS><<<(unsigned)rows, cols / E, smem, st>>>(
+        W, wdt, cols, group, rot->block, rscale, rot->signs, cb->thresholds, codes, scales, row_stride_words);
+    return launch_status();
+}
+
+template <int E>
+tq_status quantize_rows_e(const void* W, tq_dtype wdt, int64_t rows, int32_t cols, int32_t group,
+                          const tq_rotation_t* rot, const tq_codebook_t* cb, uint32_t* codes, uint16_t* scales,
+                          int64_t row_stride_words, size_t smem, float rscale, cudaStream_t st) {
+    switch (cb->levels) {
+        case 3: return quantize_rows_launch<E, 3>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 4: return quantize_rows_launch<E, 4>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 8: return quantize_rows_launch<E, 8>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 16: return quantize_rows_launch<E, 16>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
 int pick_e(int dim, int block, int group) {
     for (int e = 16; e >= 1; e >>= 1)
         if (e <= block && dim % (32 * e) == 0 && dim / e <= 1024 && group <= 32 * e) return e;
@@ -475,27 +540,17 @@ extern "C" tq_status tq_quantize(const void* W, tq_dtype wdt, int64_t rows, int3
         return launch_status();
     }
     if (e == 0 || cols > 16384) return TQ_ERR_UNSUPPORTED;
-    const int threads = cols / e;
     const size_t smem = fwht_pad_floats(cols) * 4 + 256 * 4 + (size_t)cols;
     const float rscale = (float)(1.0 / sqrt((double)rot->block));
     cudaStream_t st = as_stream(stream);
     switch (e) {
-#define TQ_Q_CASE(EE)                                                                                           \
-    case EE:                                                                                                    \
-        if (ensure_smem((const void*)quantize_rows_kernel<EE>, smem) != cudaSuccess) return TQ_ERR_CUDA;     \
-        quantize_rows_kernel<EE><<<(unsigned)rows, threads, smem, st>>>(W, wdt, cols, group, rot->block, rscale, \
-                                                                        rot->signs, cb->thresholds, cb->levels, \
-                                                                        codes, scales, row_stride_words);       \
-        break;
-        TQ_Q_CASE(1)
-        TQ_Q_CASE(2)
-        TQ_Q_CASE(4)
-        TQ_Q_CASE(8)
-        TQ_Q_CASE(16)
-#undef TQ_Q_CASE
+        case 1: return quantize_rows_e<1>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 2: return quantize_rows_e<2>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 4: return quantize_rows_e<4>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 8: return quantize_rows_e<8>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
+        case 16: return quantize_rows_e<16>(W, wdt, rows, cols, group, rot, cb, codes, scales, row_stride_words, smem, rscale, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
-    return launch_status();
 }
 
 extern "C" tq_status tq_kv_quantize(const void* k, const void* v, tq_dtype dt, int32_t T, int32_t Hkv, int32_t D,
