@@ -124,9 +124,6 @@ TQ_DEVFN float2 lds64f(uint32_t a) {
     return v;
 }
 TQ_DEVFN int pick3(const int (&a)[3], int i) { return i == 0 ? a[0] : (i == 1 ? a[1] : a[2]); }
-TQ_DEVFN int pick4(const int (&a)[kRMaxNV], int i) {
-    return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
-}
 
 // The segments as one warp sees them: record counts and first implicit pairs.
 struct RSegs {
@@ -140,6 +137,7 @@ struct RTask {
     int seg, rec, rb, ch, row, e, nv;
     bool bad;
     int pr[kRMaxNV];    // pair (output row) of each vector slot, -1 where empty
+    int vec0;           // input row of slot 0
     const uint32_t* w;  // the lane's row, first word of the chunk
 };
 
@@ -161,6 +159,7 @@ TQ_DEVFN void load_record(const RowsParams& rp, const RSegs& sg, RTask& k) {
     }
     k.bad = e < 0 || e >= p.experts;
     k.e = k.bad ? 0 : e;
+    k.vec0 = k.pr[0] < 0 ? 0 : (p.mode == kModeGather ? k.pr[0] / p.k : k.pr[0]);
 }
 
 TQ_DEVFN void set_row(const RowsParams& rp, RTask& k, int lane, int nst) {
@@ -170,17 +169,18 @@ TQ_DEVFN void set_row(const RowsParams& rp, RTask& k, int lane, int nst) {
     k.w = p.codes + (int64_t)k.e * p.expert_stride_w + (int64_t)rowc * p.row_stride + (int64_t)k.ch * nst * 8;
 }
 
-// Task t of the launch (segments in order, records, row blocks, chunks).
-TQ_DEVFN void task_of(const RowsParams& rp, const RSegs& sg, int64_t t, int lane, int nst, RTask& k) {
-    const int64_t per_rec = (int64_t)rp.row_blocks * rp.nchunks;
+// Task t of the launch (segments in order, records, row blocks, chunks; the host keeps the
+// task count below 2^31).
+TQ_DEVFN void task_of(const RowsParams& rp, const RSegs& sg, int t, int lane, int nst, RTask& k) {
+    const int per_rec = rp.row_blocks * rp.nchunks;
     int seg = 0;
-    while (seg < 2 && t >= (int64_t)pick3(sg.cnt, seg) * per_rec) {
-        t -= (int64_t)pick3(sg.cnt, seg) * per_rec;
+    while (seg < 2 && t >= pick3(sg.cnt, seg) * per_rec) {
+        t -= pick3(sg.cnt, seg) * per_rec;
         ++seg;
     }
     k.seg = seg;
-    k.rec = (int)(t / per_rec);
-    const int rem = (int)(t - (int64_t)k.rec * per_rec);
+    k.rec = t / per_rec;
+    const int rem = t - k.rec * per_rec;
     k.rb = rem / rp.nchunks;
     k.ch = rem - k.rb * rp.nchunks;
     load_record(rp, sg, k);
@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kRThreads, 1) qmv_rows_kernel(const RowsParams
 #pragma unroll
     for (int i = 0; i < 3; ++i) wsum += (int64_t)sg.cnt[i] * per_rec * seg_weight(i);
     const int64_t nw = (int64_t)gridDim.x * kRWarps, gw = (int64_t)blockIdx.x * kRWarps + warp;
-    const int64_t ta = tasks_below(sg, per_rec, wsum * gw / nw);
-    const int64_t tz = tasks_below(sg, per_rec, wsum * (gw + 1) / nw);
+    const int ta = (int)tasks_below(sg, per_rec, wsum * gw / nw);
+    const int tz = (int)tasks_below(sg, per_rec, wsum * (gw + 1) / nw);
     if (ta >= tz) return;
     const int64_t nstages = (tz - ta) * nst;
     const uint32_t lanetab = tab + (uint32_t)lane * 8u;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kRThreads, 1) qmv_rows_kernel(const RowsParams
     const uint32_t my0 = (uint32_t)lane * 32u + (swz << 4), my1 = (uint32_t)lane * 32u + ((swz ^ 1u) << 4);
 
     // stream of stages: task ts, stage ss within it
-    int64_t ts = ta;
+    int ts = ta;
     int ss = 0;
     RTask sk;
     task_of(rp, sg, ta, lane, nst, sk);
@@ -294,15 +294,21 @@ __global__ void __launch_bounds__(kRThreads, 1) qmv_rows_kernel(const RowsParams
         // the stage's input values of each vector of the record (columns past the row read as
         // zeros; cols is a multiple of 16); an empty slot is left as it is, its sums unused
         const int xcol0 = sk.ch * rp.chunk_units * U::kCodes + ss * SC;
-        const int npieces = MAXNV == 1 ? kPieces : sk.nv * kPieces;
-        for (int q = lane; q < npieces; q += 32) {
-            const int v = q / kPieces, c = q - v * kPieces;
-            const int pv = pick4(sk.pr, v);
-            if (pv < 0) continue;
-            const int vec = p.mode == kModeGather ? pv / p.k : pv;
-            const int xcol = xcol0 + 4 * c;
-            cp16(dst + kRCodeBytes + (uint32_t)(v * F::kXBytes + 16 * c),
-                 p.x + (int64_t)vec * p.cols + (xcol < p.cols ? xcol : 0), xcol < p.cols ? 16u : 0u);
+        if constexpr (MAXNV == 1) {
+            const int xcol = xcol0 + 4 * lane;
+            if (lane < kPieces)
+                cp16(dst + kRCodeBytes + 16u * (uint32_t)lane,
+                     p.x + (int64_t)sk.vec0 * p.cols + (xcol < p.cols ? xcol : 0), xcol < p.cols ? 16u : 0u);
+        } else {
+            for (int q = lane; q < sk.nv * kPieces; q += 32) {
+                const int v = q / kPieces, c = q - v * kPieces;
+                const int pv = v == 0 ? sk.pr[0] : (v == 1 ? sk.pr[1] : (v == 2 ? sk.pr[2] : sk.pr[3]));
+                if (pv < 0) continue;
+                const int vec = v == 0 ? sk.vec0 : (p.mode == kModeGather ? pv / p.k : pv);
+                const int xcol = xcol0 + 4 * c;
+                cp16(dst + kRCodeBytes + (uint32_t)(v * F::kXBytes + 16 * c),
+                     p.x + (int64_t)vec * p.cols + (xcol < p.cols ? xcol : 0), xcol < p.cols ? 16u : 0u);
+            }
         }
         if (++ss == nst) {
             ss = 0;
@@ -410,7 +416,7 @@ __global__ void __launch_bounds__(kRThreads, 1) qmv_rows_kernel(const RowsParams
         }
     };
 
-    for (int64_t t = ta; t < tz; ++t) {
+    for (int t = ta; t < tz; ++t) {
         if (t > ta) task_next(rp, sg, k, lane, nst);
         if (k.bad && lane == 0 && p.err) atomicOr(p.err, TQ_DEVERR_BAD_ID);
 #pragma unroll
