@@ -205,7 +205,14 @@ tq_status tq_qmv(const tq_qweight_t* w, const float* x_rot, int32_t T, void* y, 
  * bytes, or NULL.  Three-level books with group 16 run a table-lookup kernel
  * that splits rows wider than 2560 columns among CTAs; their partial sums go
  * to ws.  With ws NULL (or too small) such rows take the single-pass kernel
- * instead (slower); a size of 0 means no scratch is needed.
+ * instead (slower); a size of 0 means no scratch is needed.  Bit-packed books
+ * (4, 8, 16 levels) with T >= 2 and the full scratch group the T*k pairs by
+ * expert on the device, so a repeated expert's words are decoded once for up
+ * to four of its pairs; its rows wider than one column chunk also keep their
+ * partial sums in ws.  Without scratch the pairs run one by one (an f32 y then
+ * takes the chunks' sums by atomics; a bf16 y takes the single-pass kernel).
+ * Every path gives each pair the same products; only the order in which the
+ * column chunks' sums are added may differ.
  * Arithmetic of the three-level kernels: the input is held as integers per
  * group of 16 columns (|xq| <= 8191, one fp32 scale per group; the
  * single-pass kernel: 16-bit, one scale per vector); products and sums of
@@ -220,7 +227,9 @@ size_t tq_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t T, int32_t k
  * (polar_multi_gather_qmv).  y[p, :] = W_{ids[p]} x_rot[p].
  * x_rot: device f32 [P, cols].  ids: device int32 [P].  y: device [P, rows]
  * of ydt (f32 or bf16).  ws / ws_bytes and the arithmetic as for
- * tq_gather_qmv (tq_multi_gather_qmv_workspace_bytes(w, P) bytes). */
+ * tq_gather_qmv (tq_multi_gather_qmv_workspace_bytes(w, P) bytes; bit-packed
+ * books with the full scratch group the pairs by expert, each expert decoded
+ * once per record of up to four pairs). */
 tq_status tq_multi_gather_qmv(const tq_qweight_t* w, const float* x_rot, const int32_t* ids, int32_t P,
                               void* y, tq_dtype ydt, void* ws, size_t ws_bytes, uint32_t* err, void* stream);
 size_t tq_multi_gather_qmv_workspace_bytes(const tq_qweight_t* w, int32_t P);
