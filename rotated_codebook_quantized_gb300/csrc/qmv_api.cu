@@ -412,8 +412,8 @@ extern "C" tq_status tq_multi_gather_qmv_swiglu(const tq_qweight_t* w, const flo
 
 namespace {
 
-// One CTA per (selected expert, run of up to kDqRows rows), in two passes over
-// shared memory: each thread decodes whole words into one code byte per column;
+// 1-bit, ternary and 8-bit books.  One CTA per (selected expert, run of up to kDqRows rows), in
+// two passes over shared memory: each thread decodes whole words into one code byte per column;
 // then each thread writes 8 consecutive columns (one group, as 8 divides the
 // group) as a single 16-byte store for 16-bit outputs (two for f32), so a warp
 // writes 512 contiguous bytes per instruction.
@@ -491,6 +491,135 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
     }
 }
 
+// Bit-packed books (2, 3, 4 bits) in one pass: each thread writes 8 consecutive columns of one
+// row (one 16-byte store for 16-bit outputs), so a warp's stores cover 512 contiguous bytes.
+// The 8 codes come from one word, or for 3-bit books from two (a word holds 10 codes in its low
+// 30 bits, so the pair read as one 64-bit value is a contiguous run of codes); they go through a
+// per-lane table (pairs of centroids for 2- and 3-bit books, one centroid for 4-bit ones; entry
+// e of lane l at (32 e + l) entries, so a warp's lookups are conflict-free whatever the codes)
+// and are multiplied by the group's scale in fp32, as in the two-pass kernel above.
+template <int LEVELS>
+struct DqFmt {
+    static constexpr int kBits = LEVELS == 4 ? 2 : (LEVELS == 8 ? 3 : 4);
+    static constexpr int kCW = LEVELS == 8 ? 10 : 32 / kBits;  // codes per word
+    static constexpr bool kPair = LEVELS != 16;
+    static constexpr int kEntries = 1 << ((kPair ? 2 : 1) * kBits);
+    static constexpr int kEntryBytes = kPair ? 8 : 4;
+    static constexpr int kTabBytes = kEntries * 32 * kEntryBytes;
+};
+
+TQ_DEVFN float2 dq_lds64(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+TQ_DEVFN float dq_lds32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+
+// Eight consecutive outputs from element o on (a multiple of 8): one 16-byte store for 16-bit
+// outputs, two for f32.
+TQ_DEVFN void dq_store8(void* out, int odt, int64_t o, const float (&f)[8]) {
+    if (odt == TQ_F32) {
+        float4* y = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+        y[0] = make_float4(f[0], f[1], f[2], f[3]);
+        y[1] = make_float4(f[4], f[5], f[6], f[7]);
+        return;
+    }
+    uint32_t h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (odt == TQ_BF16) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * q], f[2 * q + 1]);
+            h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+        } else {
+            const __half2 b2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
+            h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+template <int LEVELS>
+__global__ void __launch_bounds__(256) dequant_bits_kernel(const uint32_t* __restrict__ codes,
+                                                           const uint16_t* __restrict__ scales, int64_t row_stride,
+                                                           int64_t esw, int64_t ess, int rows, int cols, int gshift,
+                                                           int experts, const float* __restrict__ centroids,
+                                                           const int32_t* __restrict__ ids, void* out, int odt,
+                                                           uint32_t* err) {
+    using D = DqFmt<LEVELS>;
+    constexpr int CW = D::kCW, BITS = D::kBits;
+    extern __shared__ __align__(16) uint8_t dtab[];
+    for (int i = threadIdx.x; i < D::kEntries * 32; i += blockDim.x) {
+        const int v = i >> 5;
+        if constexpr (D::kPair)
+            reinterpret_cast<float2*>(dtab)[i] =
+                make_float2(__ldg(centroids + (v & (LEVELS - 1))), __ldg(centroids + (v >> BITS)));
+        else
+            reinterpret_cast<float*>(dtab)[i] = __ldg(centroids + v);
+    }
+    __syncthreads();
+    const int vpr = cols >> 3;  // 8-column vectors per row
+    const int nvec = rows * vpr;
+    const int64_t i_sel = blockIdx.y;
+    const int e = __ldg(ids + i_sel);
+    const bool bad = e < 0 || e >= experts;
+    if (bad && err && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, TQ_DEVERR_BAD_ID);
+    const int64_t ee = bad ? 0 : e;
+    const uint32_t lbase = (uint32_t)__cvta_generic_to_shared(dtab) + (threadIdx.x & 31) * D::kEntryBytes;
+    // vectors of the selected expert's rows, strided over the CTAs of this id (the table is built
+    // once per CTA)
+    for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < nvec; f += gridDim.x * blockDim.x) {
+        const int n = f / vpr, k0 = (f - n * vpr) * 8;  // row, first column
+        const uint32_t* wrow = codes + ee * esw + (int64_t)n * row_stride;
+        const int a = k0 / CW, ob = (k0 - a * CW) * BITS;  // the first code's word and bit
+        uint32_t lo;  // the 8 codes from bit 0 on
+        if constexpr (LEVELS == 8) {
+            const uint32_t wa = __ldg(wrow + a);
+            const uint32_t wb = (ob > 6 && a + 1 < row_stride) ? __ldg(wrow + a + 1) : 0u;  // codes past word a
+            lo = (uint32_t)((((uint64_t)wb << 30) | wa) >> ob);
+        } else {
+            lo = __ldg(wrow + a) >> ob;  // 2-bit: 8 codes from bit 0 or 16; 4-bit: a whole word
+        }
+        const float sc =
+            bad ? 0.f : half_bits_to_float(__ldg(scales + ee * ess + (int64_t)n * (cols >> gshift) + (k0 >> gshift)));
+        float v8[8];
+        if constexpr (D::kPair) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t pv = (lo >> (2 * BITS * j)) & ((1u << (2 * BITS)) - 1u);
+                const float2 c = dq_lds64(lbase + (pv << 8));
+                v8[2 * j] = c.x * sc;
+                v8[2 * j + 1] = c.y * sc;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v8[q] = dq_lds32(lbase + (((lo >> (4 * q)) & 15u) << 7)) * sc;
+        }
+        dq_store8(out, odt, (i_sel * rows + n) * (int64_t)cols + k0, v8);
+    }
+}
+
+template <int LEVELS>
+tq_status launch_dequant_bits(const tq_qweight_t* w, const int32_t* ids, int32_t n_ids, void* out, tq_dtype odt,
+                              uint32_t* err, cudaStream_t st) {
+    const int64_t nvec = (int64_t)w->rows * (w->cols / 8);
+    if (nvec > 0x7fffffffll / 2) return TQ_ERR_UNSUPPORTED;
+    // about eight CTAs per SM over all ids, each looping over its id's vectors
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t per_id = std::max<int64_t>(1, (int64_t)(sms > 0 ? sms : 152) * 8 / n_ids);
+    const unsigned blocks = (unsigned)std::min<int64_t>((nvec + 255) / 256, per_id);
+    dequant_bits_kernel<LEVELS><<<dim3(blocks, (unsigned)n_ids), 256, DqFmt<LEVELS>::kTabBytes, st>>>(
+        w->codes, w->scales, w->row_stride_words, w->experts > 1 ? w->expert_stride_words : 0,
+        w->experts > 1 ? w->expert_stride_scales : 0, w->rows, w->cols, __builtin_ctz((unsigned)w->group),
+        w->experts, w->cb.centroids, ids, out, (int)odt, err);
+    return launch_status();
+}
+
 template <int LEVELS>
 tq_status launch_dequant(const tq_qweight_t* w, const int32_t* ids, int32_t n_ids, void* out, tq_dtype odt,
                          uint32_t* err, int rpc, int cpad, cudaStream_t st) {
@@ -513,17 +642,22 @@ extern "C" tq_status tq_dequant_experts(const tq_qweight_t* w, const int32_t* id
     if (n_ids < 0 || !(odt == TQ_F32 || odt == TQ_BF16 || odt == TQ_F16)) return TQ_ERR_INVALID;
     if (n_ids == 0) return TQ_OK;
     if (!ids || !out || n_ids > 65535 || !aligned(out, 16)) return TQ_ERR_INVALID;
+    cudaStream_t st = as_stream(stream);
+    // 2-, 3- and 4-bit books: one pass, one 8-column store per thread
+    switch (w->cb.levels) {
+        case 4: return launch_dequant_bits<4>(w, ids, n_ids, out, odt, err, st);
+        case 8: return launch_dequant_bits<8>(w, ids, n_ids, out, odt, err, st);
+        case 16: return launch_dequant_bits<16>(w, ids, n_ids, out, odt, err, st);
+        default: break;
+    }
+    // the others (1-bit, ternary, 8-bit books): the two-pass kernel
     const int cw = host_codes_per_word(w->cb.levels);
     const int cpad = (int)((tq_row_words(w->cb.levels, w->cols) * cw + 15) / 16 * 16);
     if (cpad > 160 * 1024) return TQ_ERR_UNSUPPORTED;
     const int rpc = std::max(1, std::min(kDqRows, 40960 / cpad));
-    cudaStream_t st = as_stream(stream);
     switch (w->cb.levels) {
         case 2: return launch_dequant<2>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
         case 3: return launch_dequant<3>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
-        case 4: return launch_dequant<4>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
-        case 8: return launch_dequant<8>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
-        case 16: return launch_dequant<16>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
         case 256: return launch_dequant<256>(w, ids, n_ids, out, odt, err, rpc, cpad, st);
         default: return TQ_ERR_UNSUPPORTED;
     }
