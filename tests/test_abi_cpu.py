@@ -131,3 +131,35 @@ def test_qmv_tc_host_checks_and_workspace():
     assert lib.tq_qmv_tc(ctypes.byref(rows130), fake, 3, fake, fake, need, None, None) == tq.TQ_ERR_UNSUPPORTED
     cols96 = tq.tq_qweight_t(fake.value, fake.value, 1, 256, 96, 32, 12, 0, 0, cb8)
     assert lib.tq_qmv_tc(ctypes.byref(cols96), fake, 3, fake, fake, need, None, None) == tq.TQ_ERR_UNSUPPORTED
+
+
+def test_gather_workspace_sizes_cover_grouping():
+    """Scratch sizes of the bit-packed gathers (host only): with more than one token, or per-pair
+    inputs, the size adds the record lists of the grouping (whole 256-byte pieces, at least a
+    count per expert and an id per pair) to the per-pair partial sums; one token, and ternary
+    books, need no lists."""
+    import rotated_codebook_quantized_gb300 as tq
+
+    lib = tq.load()
+    fake = ctypes.c_void_p(0x1000)
+    E, rows, cols, group = 128, 4096, 1536, 64
+    stride = (o.row_words(8, cols) + 3) // 4 * 4
+    cb8 = tq.tq_codebook_t(8, fake.value, fake.value)
+    qw = tq.tq_qweight_t(fake.value, fake.value, E, rows, cols, group, stride, rows * stride,
+                         rows * (cols // group), cb8)
+    P = 64
+    one_token = lib.tq_gather_qmv_workspace_bytes(ctypes.byref(qw), 1, P)
+    eight_tokens = lib.tq_gather_qmv_workspace_bytes(ctypes.byref(qw), 8, P // 8)
+    multi = lib.tq_multi_gather_qmv_workspace_bytes(ctypes.byref(qw), P)
+    lists = eight_tokens - one_token
+    assert multi == eight_tokens
+    assert lists > 0 and lists % 256 == 0 and lists >= 4 * (E + 2 * P)
+    assert lib.tq_gather_qmv_workspace_bytes(ctypes.byref(qw), 0, 8) == 0
+    assert lib.tq_multi_gather_qmv_workspace_bytes(ctypes.byref(qw), 0) == 0
+    cb3 = tq.tq_codebook_t(3, fake.value, fake.value)
+    stride3 = (o.row_words(3, 7168) + 3) // 4 * 4
+    tw = tq.tq_qweight_t(fake.value, fake.value, 16, 2048, 7168, 16, stride3, 2048 * stride3, 2048 * 448, cb3)
+    assert lib.tq_gather_qmv_workspace_bytes(ctypes.byref(tw), 8, 8) == \
+        lib.tq_gather_qmv_workspace_bytes(ctypes.byref(tw), 1, 64)
+    assert lib.tq_multi_gather_qmv_workspace_bytes(ctypes.byref(tw), 64) == \
+        lib.tq_gather_qmv_workspace_bytes(ctypes.byref(tw), 1, 64)
